@@ -1,6 +1,237 @@
 """Quantized GEMV with fused dequantization for GB300 (sm_103a).
 
 The compute lives in the CUDA library libqgemv.so (C ABI in include/qgemv.h);
-this package is a thin ctypes binding over it. The library is loaded on first
-use: every call fails loudly if it has not been built or no GPU is present.
+this module is a thin ctypes binding over it with the same names. It only
+marshals arguments: torch supplies device memory and the current stream,
+every step of the computation runs in the library's kernels. The library is
+loaded on first use, and every call raises if it has not been built or no
+CUDA device is present: there is no CPU fallback.
+
+Workspace: calls that need device scratch (split-K partial sums) get it from
+a per-device torch buffer that grows on demand, unless the caller passes one.
 """
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemv.so")
+
+QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_MISALIGNED = 0, 1, 2, 3
+QG_ERR_CUDA, QG_ERR_WORKSPACE, QG_ERR_DEVICE = 4, 5, 6
+QG_OP_Q4_0, QG_OP_DUAL_Q4_0, QG_OP_Q4_K, QG_OP_AFFINE = 0, 1, 2, 3
+
+EXPORTS = ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_split",
+           "dequant_q4_0", "dequant_q4_k", "dequant_affine", "qg_workspace_size",
+           "qg_status_string", "qg_last_cuda_error", "qg_device_error",
+           "qg_selftest_wait_timeout")
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+class QGError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        self.status = status
+        msg = f"{what}: {status_string(status)}"
+        if status == QG_ERR_CUDA:
+            msg += f" (cudaError {lib().qg_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def lib():
+    """The loaded library (ctypes.CDLL), typed. Raises if it was not built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = C.CDLL(LIB_PATH)
+        P, I64, I, SZ = C.c_void_p, C.c_int64, C.c_int, C.c_size_t
+        sig = {
+            "qgemv_q4_0": [P, P, P, I64, I64, I64, P, SZ, P],
+            "qgemv_dual_q4_0": [P, P, P, P, P, I64, I64, I64, P, SZ, P],
+            "qgemv_q4_k": [P, P, P, I64, I64, I64, P, SZ, P],
+            "qmm_affine": [P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P],
+            "qkv_split": [P, P, P, P, I64, I64, I64, I64, P],
+            "dequant_q4_0": [P, P, I64, I64, P],
+            "dequant_q4_k": [P, P, I64, I64, P],
+            "dequant_affine": [P, P, P, P, I64, I64, I, I, P],
+            "qg_workspace_size": [I, I64, I64, I64, I, I, C.POINTER(SZ)],
+            "qg_status_string": [I],
+            "qg_last_cuda_error": [],
+            "qg_device_error": [I, C.POINTER(C.c_uint)],
+            "qg_selftest_wait_timeout": [I64, P],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = C.c_char_p if name == "qg_status_string" else C.c_int
+        _LIB = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().qg_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != QG_OK:
+        raise QGError(what, rc)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# --------------------------------------------------------------- workspace
+_WS = {}
+
+
+def workspace_size(op: int, M: int, N: int, K: int, group_size: int = 0, packed: int = 0) -> int:
+    n = C.c_size_t(0)
+    _check(lib().qg_workspace_size(op, M, N, K, group_size, packed, C.byref(n)), "qg_workspace_size")
+    return int(n.value)
+
+
+def _workspace(op, M, N, K, gs, packed, device, workspace):
+    need = workspace_size(op, M, N, K, gs, packed)
+    if workspace is not None:
+        return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    if need == 0:
+        return None, 0
+    key = torch.device(device).index
+    buf = _WS.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(need, dtype=torch.uint8, device=device)
+        _WS[key] = buf
+    return buf.data_ptr(), buf.numel()
+
+
+# ------------------------------------------------------------------- calls
+def qgemv_q4_0(w, x, y=None, *, N=None, workspace=None, stream=None):
+    """y[M,N] = x[M,K] . dequant_q4_0(w)^T. w: uint8 Q4_0 bytes of N rows."""
+    M, K = x.shape
+    N = N if N is not None else w.numel() // (K // 32 * 18)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(QG_OP_Q4_0, M, N, K, 0, 0, x.device, workspace)
+    _check(lib().qgemv_q4_0(_dev(w, "w", torch.uint8), _dev(x, "x", torch.float32),
+                            _dev(y, "y", torch.float32), M, N, K, ws, wsb, _stream(stream)),
+           "qgemv_q4_0")
+    return y
+
+
+def qgemv_dual_q4_0(w_a, w_b, x, y_a=None, y_b=None, *, N=None, workspace=None, stream=None):
+    """(y_a, y_b) = (x . dequant(w_a)^T, x . dequant(w_b)^T) in one launch."""
+    M, K = x.shape
+    N = N if N is not None else w_a.numel() // (K // 32 * 18)
+    if y_a is None:
+        y_a = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if y_b is None:
+        y_b = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(QG_OP_DUAL_Q4_0, M, N, K, 0, 0, x.device, workspace)
+    _check(lib().qgemv_dual_q4_0(_dev(w_a, "w_a", torch.uint8), _dev(w_b, "w_b", torch.uint8),
+                                 _dev(x, "x", torch.float32), _dev(y_a, "y_a", torch.float32),
+                                 _dev(y_b, "y_b", torch.float32), M, N, K, ws, wsb,
+                                 _stream(stream)), "qgemv_dual_q4_0")
+    return y_a, y_b
+
+
+def qgemv_q4_k(w, x, y=None, *, N=None, workspace=None, stream=None):
+    """y[M,N] = x[M,K] . dequant_q4_k(w)^T. w: uint8 Q4_K bytes of N rows."""
+    M, K = x.shape
+    N = N if N is not None else w.numel() // (K // 256 * 144)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(QG_OP_Q4_K, M, N, K, 0, 0, x.device, workspace)
+    _check(lib().qgemv_q4_k(_dev(w, "w", torch.uint8), _dev(x, "x", torch.float32),
+                            _dev(y, "y", torch.float32), M, N, K, ws, wsb, _stream(stream)),
+           "qgemv_q4_k")
+    return y
+
+
+def qmm_affine(x, q, scales, biases, group_size, packed, y=None, *, workspace=None, stream=None):
+    """y = x . dequant_affine(q, scales, biases)^T; q uint8 codes ([N,K] or [N,K/2])."""
+    M, K = x.shape
+    N = scales.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(QG_OP_AFFINE, M, N, K, group_size, int(packed), x.device, workspace)
+    _check(lib().qmm_affine(_dev(x, "x", torch.float32), _dev(q, "q", torch.uint8),
+                            _dev(scales, "scales", torch.float32),
+                            _dev(biases, "biases", torch.float32), _dev(y, "y", torch.float32),
+                            M, N, K, int(group_size), int(packed), ws, wsb, _stream(stream)),
+           "qmm_affine")
+    return y
+
+
+def qkv_split(qkv, q_sp, k_sp, v_sp, q=None, k=None, v=None, *, stream=None):
+    """Split [seq, q_sp+k_sp+v_sp] f32 into q [seq,q_sp], k [seq,k_sp], v [seq,v_sp]."""
+    seq = qkv.shape[0]
+    dev = qkv.device
+    q = torch.empty((seq, q_sp), dtype=torch.float32, device=dev) if q is None else q
+    k = torch.empty((seq, k_sp), dtype=torch.float32, device=dev) if k is None else k
+    v = torch.empty((seq, v_sp), dtype=torch.float32, device=dev) if v is None else v
+    _check(lib().qkv_split(_dev(qkv, "qkv", torch.float32), _dev(q, "q", torch.float32),
+                           _dev(k, "k", torch.float32), _dev(v, "v", torch.float32), seq, q_sp,
+                           k_sp, v_sp, _stream(stream)), "qkv_split")
+    return q, k, v
+
+
+def dequant_q4_0(w, N, K, out=None, *, stream=None):
+    out = torch.empty((N, K), dtype=torch.float32, device=w.device) if out is None else out
+    _check(lib().dequant_q4_0(_dev(w, "w", torch.uint8), _dev(out, "out", torch.float32), N, K,
+                              _stream(stream)), "dequant_q4_0")
+    return out
+
+
+def dequant_q4_k(w, N, K, out=None, *, stream=None):
+    out = torch.empty((N, K), dtype=torch.float32, device=w.device) if out is None else out
+    _check(lib().dequant_q4_k(_dev(w, "w", torch.uint8), _dev(out, "out", torch.float32), N, K,
+                              _stream(stream)), "dequant_q4_k")
+    return out
+
+
+def dequant_affine(q, scales, biases, N, K, group_size, packed, out=None, *, stream=None):
+    out = torch.empty((N, K), dtype=torch.float32, device=q.device) if out is None else out
+    _check(lib().dequant_affine(_dev(q, "q", torch.uint8), _dev(scales, "scales", torch.float32),
+                                _dev(biases, "biases", torch.float32),
+                                _dev(out, "out", torch.float32), N, K, int(group_size),
+                                int(packed), _stream(stream)), "dequant_affine")
+    return out
+
+
+def device_error(clear: bool = True) -> int:
+    """Synchronize and return (optionally clearing) the device error word."""
+    code = C.c_uint(0)
+    rc = lib().qg_device_error(int(clear), C.byref(code))
+    if rc not in (QG_OK, QG_ERR_DEVICE):
+        raise QGError("qg_device_error", rc)
+    return int(code.value)
+
+
+def selftest_wait_timeout(timeout_ns: int, *, stream=None):
+    _check(lib().qg_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
+           "qg_selftest_wait_timeout")

@@ -1,0 +1,143 @@
+// Internal declarations shared by the library's translation units:
+// inline-PTX helpers (mbarrier, 1-D TMA bulk copy, timers) and the launchers
+// each .cu file exports to the C-ABI layer in qg_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qgemv.h"
+
+namespace qg {
+
+// ---------------------------------------------------------------- error codes
+// Codes a kernel writes into the per-device error word (bit mask).
+enum : unsigned {
+    DEVERR_WAIT_FULL = 1u,      // consumer gave up waiting for a stage to land
+    DEVERR_WAIT_EMPTY = 2u,     // producer gave up waiting for a stage to drain
+    DEVERR_WAIT_DRAIN = 4u,     // copies still in flight after an error
+    DEVERR_SELFTEST = 8u,       // the self-test wait ran out (expected)
+};
+
+// Bounded waits give up after this many nanoseconds.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete; false after
+// `limit_ns` without completion (the caller then records an error).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// L2 policy for data read exactly once (weights): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D TMA bulk copy global -> shared, completion signalled on `bar` as
+// transaction bytes. dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void report_error(unsigned* err, unsigned code) {
+    if (err) atomicOr(err, code);
+}
+
+// ----------------------------------------------------------- launch plumbing
+struct DevCtx {
+    int device;
+    int num_sms;
+    int max_smem_optin;   // bytes of dynamic shared memory a block may opt into
+    unsigned* err;        // device address of this device's error word
+};
+
+// ----------------------------------------------------------------- launchers
+// GEMV family (gemv.cu). fmt: see GemvFmt. Returns a qg_status.
+enum GemvFmt : int { FMT_Q4_0 = 0, FMT_Q4_K = 1, FMT_AFF_U8 = 2, FMT_AFF_PACKED = 3 };
+
+struct GemvArgs {
+    int fmt;
+    int nw;                    // 1, or 2 for the fused dual projection
+    const uint8_t* w[2];
+    float* y[2];
+    const float* x;
+    const float* scales;       // affine only
+    const float* biases;       // affine only
+    int64_t M, N, K;
+    int gs;                    // affine only
+};
+
+size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a);
+int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// Copies and dequantization (elementwise.cu).
+int qkv_split_launch(const DevCtx& dc, const float* qkv, float* q, float* k, float* v,
+                     int64_t seq, int64_t q_sp, int64_t k_sp, int64_t v_sp, cudaStream_t s);
+int dequant_launch(const DevCtx& dc, int fmt, const uint8_t* w, const float* scales,
+                   const float* biases, float* out, int64_t N, int64_t K, int gs,
+                   cudaStream_t s);
+int selftest_wait_launch(const DevCtx& dc, long long timeout_ns, cudaStream_t s);
+
+// Record a CUDA error for qg_last_cuda_error() and return QG_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+
+}  // namespace qg

@@ -1,0 +1,170 @@
+/*
+ * qgemv.h - C ABI of libqgemv.so: quantized matrix-vector and skinny matmul
+ * with fused dequantization, for NVIDIA GB300 (sm_103a).
+ *
+ *   y[M, N] = x[M, K] . dequant(W)[N, K]^T      (f32 in, f32 out)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All pointers are DEVICE pointers owned by the caller; the library keeps
+ *   none of them after the call returns. Row-major, densely packed.
+ * - Calls are asynchronous: they enqueue work on `stream` (NULL = the legacy
+ *   default stream) and return. Results are valid once the stream is
+ *   synchronized. Nothing is allocated on the device by these calls.
+ * - Every call validates its arguments first; on a validation failure it
+ *   enqueues nothing and returns a non-zero qg_status. A failed launch
+ *   returns QG_ERR_CUDA (qg_last_cuda_error() gives the cudaError_t).
+ * - Buffer lengths cannot be checked through raw pointers: the sizes stated
+ *   below are preconditions. Outputs must not overlap inputs or each other.
+ * - Alignment: x, y, scales and biases need 4-byte alignment (else
+ *   QG_ERR_MISALIGNED); weights may start at any byte.
+ *   The fastest path additionally wants 16-byte aligned weight rows
+ *   (K % 256 == 0 and 16-byte aligned base pointers); otherwise a slower
+ *   general kernel computes the same result within the same tolerance.
+ * - Accuracy: every f32 output y satisfies |y - ref| <= 1e-5 * B + 1e-6 where
+ *   ref is the exact dot product of x with the dequantized weights and
+ *   B = sum_k |x_k w_k| (the tensor-core prefill path: 2e-3 * B + 1e-6).
+ *   Dequantization exports are bit-exact.
+ * - Workspace: the GEMV/qmm calls may need device scratch for a deterministic
+ *   split-K reduction or a prefill prologue. Query the size with
+ *   qg_workspace_size(); pass a buffer at least that large (16-byte aligned),
+ *   or NULL/0 when the size is 0. Too small a buffer returns
+ *   QG_ERR_WORKSPACE. Calls that share one workspace must not overlap.
+ *
+ * Formats
+ * -------
+ * Q4_0   (page: fused_dual_proj_q4_0.rs, mlx-native 0.9.1, preconditions of
+ *        dispatch_fused_dual_proj_q4_0): 32 weights per 18-byte block, fp16 d
+ *        (little-endian) then 16 bytes; byte 2+j holds element j in its low
+ *        nibble and element 16+j in its high nibble; w = (q - 8) * d. Weight
+ *        matrix = N rows of K/32 blocks. Requires K % 32 == 0.
+ * Q4_K   (page: q4_k_gemv_v2.rs, ferrum-kernels 0.7.7, module doc):
+ *        256 weights per 144-byte super-block: fp16 d, fp16 dmin, 12 bytes of
+ *        packed 6-bit (scale, min) pairs for 8 sub-blocks of 32, 128 nibble
+ *        bytes (chunk c of 32 bytes: low nibbles = sub-block 2c, high nibbles
+ *        = sub-block 2c+1); w = (d*sc)*q - dmin*m. N rows of K/256
+ *        super-blocks. Requires K % 256 == 0.
+ * affine (page: qmm_affine.rs, mlx-native 0.21.1, qmm_affine_t_cpu and
+ *        pack_b4_to_u32): w[n,k] = fma(q[n,k], s[n,g], b[n,g]), g = k / gs,
+ *        gs a power of two in [2, 1024], K % gs == 0. Codes are one u8 per
+ *        element ([N, K] bytes, packed = 0) or two 4-bit codes per byte
+ *        ([N, K/2] bytes, element 2i in the low nibble of byte i, packed = 1,
+ *        K even). s, b: f32 [N, K/gs].
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA
+ * header. */
+typedef struct CUstream_st* qg_stream_t;
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = 1,   /* zero/negative dims, bad divisibility, NULL, aliasing */
+    QG_ERR_UNSUPPORTED = 2,   /* valid request outside what this build supports */
+    QG_ERR_MISALIGNED = 3,    /* pointer alignment below the stated minimum */
+    QG_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    QG_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */
+    QG_ERR_DEVICE = 6         /* a kernel reported an error (see qg_device_error) */
+} qg_status;
+
+/* Operation ids for qg_workspace_size. */
+enum {
+    QG_OP_Q4_0 = 0,
+    QG_OP_DUAL_Q4_0 = 1,
+    QG_OP_Q4_K = 2,
+    QG_OP_AFFINE = 3
+};
+
+/* Single Q4_0 projection: y[M,N] = x[M,K] . dequant(w)[N,K]^T.
+ * Page: fused_dual_proj_q4_0.rs (mlx-native 0.9.1) - the baseline
+ * kernel_mul_mv_q4_0_f32 dispatch the fused op is defined against.
+ * w: N*(K/32)*18 bytes; x: M*K f32; y: M*N f32. M, N, K > 0, K % 32 == 0. */
+QG_API int qgemv_q4_0(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
+               void* workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/* Fused dual Q4_0 projection: two weights of equal shape share one input.
+ * Page: fused_dual_proj_q4_0.rs (mlx-native 0.9.1), dispatch_fused_dual_proj_q4_0
+ * ("byte-identical to two kernel_mul_mv_q4_0_f32 dispatches").
+ * y_a = x . dequant(w_a)^T, y_b = x . dequant(w_b)^T; each output is bitwise
+ * equal to what qgemv_q4_0 returns for the same weight when both weights
+ * take the same path (same alignment class). Sizes as for qgemv_q4_0;
+ * y_a != y_b. */
+QG_API int qgemv_dual_q4_0(const void* w_a, const void* w_b, const float* x, float* y_a, float* y_b,
+                    int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                    qg_stream_t stream);
+
+/* Q4_K GEMV. Page: q4_k_gemv_v2.rs (ferrum-kernels 0.7.7),
+ * dispatch_gemv_q4k_v2_offset (M = 1 there; any M here).
+ * w: N*(K/256)*144 bytes; x: M*K f32; y: M*N f32. K % 256 == 0. Callers that
+ * keep several tensors in one buffer pass offset pointers (byte offsets
+ * must keep the stated alignment). */
+QG_API int qgemv_q4_k(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
+               void* workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/* Affine group-quantized matmul y = x . dequant(q, s, b)^T.
+ * Page: qmm_affine.rs (mlx-native 0.21.1), dispatch_qmm_affine_t_f32 and
+ * dispatch_qmm_affine_t_packed_simd4_b4 (packed 4-bit codes). The packed and
+ * one-code-per-byte storages give bitwise-identical y. M up to 8 runs on CUDA
+ * cores; larger M is a prefill contraction. */
+QG_API int qmm_affine(const float* x, const void* q, const float* scales, const float* biases, float* y,
+               int64_t M, int64_t N, int64_t K, int group_size, int packed, void* workspace,
+               size_t workspace_bytes, qg_stream_t stream);
+
+/* Split a fused [seq, q_sp + k_sp + v_sp] f32 tensor into q [seq, q_sp],
+ * k [seq, k_sp], v [seq, v_sp]. Page: qkv_split.rs (mlx-native 0.7.1),
+ * dispatch_qkv_split_f32. A bit copy: every 32-bit word, NaN payloads
+ * included, lands unchanged in exactly one output. All spans > 0; their sum
+ * must not overflow. */
+QG_API int qkv_split(const float* qkv, float* q, float* k, float* v, int64_t seq, int64_t q_sp,
+              int64_t k_sp, int64_t v_sp, qg_stream_t stream);
+
+/* Dequantize a whole weight matrix to f32 out[N, K], bit-exact with the
+ * format definition. Page: qmm_affine.rs (mlx-native 0.21.1), the
+ * qdq_affine forward composition test (dequantize, then matmul). */
+QG_API int dequant_q4_0(const void* w, float* out, int64_t N, int64_t K, qg_stream_t stream);
+QG_API int dequant_q4_k(const void* w, float* out, int64_t N, int64_t K, qg_stream_t stream);
+QG_API int dequant_affine(const void* q, const float* scales, const float* biases, float* out,
+                   int64_t N, int64_t K, int group_size, int packed, qg_stream_t stream);
+
+/* Workspace bytes op (QG_OP_*) needs for the given shape; *bytes = 0 when
+ * none. group_size/packed matter only for QG_OP_AFFINE. Returns a status. */
+QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_size, int packed,
+                      size_t* bytes);
+
+/* Human-readable text of a qg_status. Never NULL. */
+QG_API const char* qg_status_string(int status);
+
+/* cudaError_t of the most recent QG_ERR_CUDA on this host thread. */
+QG_API int qg_last_cuda_error(void);
+
+/* Kernels never trap: a kernel that gives up on a bounded wait records a
+ * non-zero code in a per-device error word instead. This call synchronizes
+ * the current device, reads the word into *code (may be NULL) and clears it
+ * when clear != 0. Returns QG_OK, or QG_ERR_DEVICE when the word was
+ * non-zero. */
+QG_API int qg_device_error(int clear, unsigned int* code);
+
+/* Self-test of the bounded wait: launches one block that waits on a barrier
+ * nobody arrives at for about timeout_ns nanoseconds (capped at 2 s), then
+ * records its timeout code in the device error word and exits. */
+QG_API int qg_selftest_wait_timeout(int64_t timeout_ns, qg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports every symbol include/qgemv.h
+declares; host-side validation rejects bad arguments without touching a GPU
+(CPU only: no compute call is made)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_quantized_gemv_dequant_gb300 import _build
+    path = _build.build()
+    return C.CDLL(path)
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "qgemv.h")) as f:
+        text = f.read()
+    return re.findall(r"QG_API\s+(?:const\s+)?\w+\*?\s+(\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_symbols())
+    for n in ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_split",
+              "dequant_q4_0", "dequant_q4_k", "dequant_affine"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_binding_names_match_header():
+    import bit_quantized_gemv_dequant_gb300 as qg
+    assert set(qg.EXPORTS) == set(declared_symbols())
+
+
+def test_status_strings(lib):
+    lib.qg_status_string.restype = C.c_char_p
+    assert lib.qg_status_string(0) == b"ok"
+    assert lib.qg_status_string(1) == b"invalid argument"
+    assert lib.qg_status_string(99) == b"unknown status"
+
+
+def test_validation_needs_no_gpu(lib):
+    P, I64 = C.c_void_p, C.c_int64
+    f = lib.qgemv_q4_0
+    f.argtypes = [P, P, P, I64, I64, I64, P, C.c_size_t, P]
+    fake = 0x10000
+    # zero M, K not a multiple of 32, NULL weight, output aliasing input
+    assert f(fake, fake + 4096, fake + 8192, 0, 4, 64, None, 0, None) == 1
+    assert f(fake, fake + 4096, fake + 8192, 1, 4, 48, None, 0, None) == 1
+    assert f(None, fake + 4096, fake + 8192, 1, 4, 64, None, 0, None) == 1
+    assert f(fake, fake + 4096, fake + 4096, 1, 4, 64, None, 0, None) == 1
+    assert f(fake, fake + 4098, fake + 8192, 1, 4, 64, None, 0, None) == 3  # x misaligned
+    g = lib.qmm_affine
+    g.argtypes = [P, P, P, P, P, I64, I64, I64, C.c_int, C.c_int, P, C.c_size_t, P]
+    assert g(fake, fake + 4096, fake + 8192, fake + 12288, fake + 16384, 1, 4, 64, 48, 0,
+             None, 0, None) == 1  # group size not a power of two
+    assert g(fake, fake + 4096, fake + 8192, fake + 12288, fake + 16384, 1, 4, 64, 2048, 0,
+             None, 0, None) == 1  # group size above 1024
+    assert g(fake, fake + 4096, fake + 8192, fake + 12288, fake + 16384, 1, 4, 63, 64, 1,
+             None, 0, None) == 1
+    h = lib.qkv_split
+    h.argtypes = [P, P, P, P, I64, I64, I64, I64, P]
+    assert h(fake, fake + 4096, fake + 8192, fake + 12288, 4, 0, 1, 1, None) == 1
+    assert h(fake, fake + 4096, fake + 8192, fake + 12288, 4, 2**62, 2**62, 1, None) == 1
+    k = lib.qgemv_q4_k
+    k.argtypes = [P, P, P, I64, I64, I64, P, C.c_size_t, P]
+    assert k(fake, fake + 4096, fake + 8192, 1, 4, 128, None, 0, None) == 1  # K % 256
