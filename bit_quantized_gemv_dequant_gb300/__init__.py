@@ -24,11 +24,12 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_MISALIGNED = 0, 1, 2, 3
 QG_ERR_CUDA, QG_ERR_WORKSPACE, QG_ERR_DEVICE = 4, 5, 6
 QG_OP_Q4_0, QG_OP_DUAL_Q4_0, QG_OP_Q4_K, QG_OP_AFFINE = 0, 1, 2, 3
+QG_OPT_PDL = 1
 
 EXPORTS = ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_split",
            "dequant_q4_0", "dequant_q4_k", "dequant_affine", "qg_workspace_size",
            "qg_status_string", "qg_last_cuda_error", "qg_device_error",
-           "qg_selftest_wait_timeout")
+           "qg_selftest_wait_timeout", "qg_set_option", "qg_get_option")
 
 _LIB = None
 _LOCK = threading.Lock()
@@ -69,6 +70,8 @@ def lib():
             "qg_last_cuda_error": [],
             "qg_device_error": [I, C.POINTER(C.c_uint)],
             "qg_selftest_wait_timeout": [I64, P],
+            "qg_set_option": [I, I64],
+            "qg_get_option": [I, C.POINTER(I64)],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -235,3 +238,14 @@ def device_error(clear: bool = True) -> int:
 def selftest_wait_timeout(timeout_ns: int, *, stream=None):
     _check(lib().qg_selftest_wait_timeout(int(timeout_ns), _stream(stream)),
            "qg_selftest_wait_timeout")
+
+
+def set_option(option: int, value: int):
+    """qg_set_option: e.g. set_option(QG_OPT_PDL, 1) (see include/qgemv.h)."""
+    _check(lib().qg_set_option(int(option), int(value)), "qg_set_option")
+
+
+def get_option(option: int) -> int:
+    v = C.c_int64(0)
+    _check(lib().qg_get_option(int(option), C.byref(v)), "qg_get_option")
+    return int(v.value)

@@ -1,403 +1,38 @@
-// Dequantize-fused GEMV / skinny matmul on CUDA cores (M <= 8 per launch).
+// GEMV / skinny-matmul dispatch (M <= 8 per launch; larger M is processed in
+// slices of 8 rows of x): planning of the fast kernel of gemv_fast.cuh, the
+// general kernel for shapes and alignments the fast one does not take, and
+// the deterministic split-K finalization.
 //
 // Pages: fused_dual_proj_q4_0.rs (mlx-native 0.9.1), q4_k_gemv_v2.rs
-// (ferrum-kernels 0.7.7) and qmm_affine.rs (mlx-native 0.21.1) define the
-// operations and their host contracts; their Metal kernels (64-thread
-// threadgroups, two rows per simdgroup) are not reused. This design is
-// written for sm_103a:
+// (ferrum-kernels 0.7.7), qmm_affine.rs (mlx-native 0.21.1).
 //
-//  * One persistent CTA per SM (8 consumer warps + 1 producer warp). The CTAs
-//    split the list of row chunks (R consecutive rows of one weight matrix)
-//    into contiguous, balanced ranges.
-//  * The producer streams each chunk's bytes from HBM into a ring of shared
-//    memory stages with 1-D TMA bulk copies (cp.async.bulk, evict-first L2
-//    policy) completing on mbarriers, so a whole SM's share of the weights
-//    can be in flight at once without holding registers.
-//  * x (one k-slice of it) is staged once per CTA in shared memory, permuted
-//    so that each lane's 8 inputs for a 256-element pass are two conflict-free
-//    float4 loads. A warp loads them into registers once per pass and reuses
-//    them for the R rows of its chunk and all M inputs.
-//  * Nibbles become exact floats with an exponent-bias trick (OR into the
-//    mantissa of 2^23, subtract), are multiplied by x in f32, and the per-
-//    block scale is applied once per lane-block. Partial sums of the R*M
-//    outputs are reduced across the warp with a transposing butterfly.
-//  * When x does not fit (M*K*4 > 128 KB) the grid also splits K into KS
-//    slices; each slice writes partial sums to the workspace and a second
-//    kernel adds them in slice order, so results stay deterministic.
-//
-// Every output's arithmetic depends only on (format, M bucket, K, KS), never
-// on which CTA, warp or chunk computed it, so the dual projection is bitwise
-// equal to two single projections.
+// Split-K: when x for the M inputs does not fit in shared memory next to the
+// weight stages (M*K*4 > 128 KB), the grid also splits K into KS slices. Each
+// slice writes partial sums to the caller's workspace and splitk_finalize adds
+// them in slice order, so results are deterministic and independent of the
+// launch geometry.
 #include <cuda_fp16.h>
 
 #include <algorithm>
 
+#include "gemv_fast.cuh"
 #include "qg_internal.cuh"
 
 namespace qg {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
-constexpr int kPass = 256;            // K elements per lane-pass (32 lanes x 8)
-constexpr int kMaxStages = 24;
-constexpr size_t kXMaxBytes = 128 * 1024;
-
 struct KParams {
     const uint8_t* w[2];
-    float* out[2];            // y (KS == 1) or unused (KS > 1: partial)
-    float* partial;           // [KS][nw][M][N] when KS > 1
+    float* out[2];
     const float* x;
     const float* s;
     const float* b;
     int M, N, K;
     int log2gs;
     int nw;
-    int klen, passes;
-    int chunks_per_w, total_chunks;
-    int S, stage_bytes;
-    int q_stride, sb_stride, sb_off;
     long long q_row_bytes;
     int G;                    // groups per full row (affine)
-    int KS;
-    unsigned* err;
 };
-
-__host__ __device__ constexpr int q_bytes_per_pass(int fmt) {
-    return fmt == FMT_AFF_U8 ? 256 : (fmt == FMT_AFF_PACKED ? 128 : 144);
-}
-
-// Exact float of a small code q (< 2^23): 2^23 + q, minus 2^23 (+ bias).
-__device__ __forceinline__ float code_f(uint32_t q) {
-    return __int_as_float(0x4B000000u | q) - 8388608.0f;
-}
-__device__ __forceinline__ float code_f_minus8(uint32_t q) {
-    return __int_as_float(0x4B000000u | q) - 8388616.0f;
-}
-
-// Position in the permuted x layout of element e (0 <= e < klen) of input m:
-// [m][pass][plane][lane][4]; each lane reads its 8 values as two float4.
-template <int FMT>
-__device__ __forceinline__ int x_index(int m, int e, int passes) {
-    const int pp = e >> 8, ee = e & 255;
-    int plane, lane, t;
-    if (FMT == FMT_Q4_0) {
-        const int j = ee & 31;
-        plane = j >> 4;
-        lane = (ee >> 5) * 4 + ((j & 15) >> 2);
-        t = j & 3;
-    } else if (FMT == FMT_Q4_K) {
-        const int j = ee & 63;
-        plane = j >> 5;
-        lane = (ee >> 6) * 8 + ((j & 31) >> 2);
-        t = j & 3;
-    } else {
-        lane = ee >> 3;
-        plane = (ee >> 2) & 1;
-        t = ee & 3;
-    }
-    return (((m * passes + pp) * 2 + plane) * 32 + lane) * 4 + t;
-}
-
-// The (scale, min) 6-bit pair of sub-block j from the 12 packed bytes held
-// as three little-endian words.
-__device__ __forceinline__ void q4k_pair(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc,
-                                         int& mn) {
-    const int jj = j & 3, sh = 8 * jj;
-    const uint32_t b0 = (s0 >> sh) & 0xFF, b1 = (s1 >> sh) & 0xFF, b2 = (s2 >> sh) & 0xFF;
-    if (j < 4) {
-        sc = b0 & 63;
-        mn = b1 & 63;
-    } else {
-        sc = (b2 & 15) | ((b0 >> 6) << 4);
-        mn = (b2 >> 4) | ((b1 >> 6) << 4);
-    }
-}
-
-// Warp reduction of V values at once. Afterwards lane l holds the full sum
-// of value l / (32 / V). Each value is summed over the same xor-butterfly
-// tree as a plain one-value reduction.
-template <int V>
-__device__ __forceinline__ void butterfly(float (&v)[V], int lane) {
-    int cur = V;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        if (cur > 1) {
-            const int half = cur / 2;
-            const bool upper = (lane & off) != 0;
-#pragma unroll
-            for (int i = 0; i < V / 2; ++i) {
-                if (i < half) {
-                    const float send = upper ? v[i] : v[i + half];
-                    const float keep = upper ? v[i + half] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-            }
-            cur = half;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-        }
-    }
-}
-
-template <int FMT, int MT, int R>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const KParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    float* xs = reinterpret_cast<float*>(smem);
-    const int x_bytes = (MT * p.klen * 4 + 127) & ~127;
-    uint8_t* stages = smem + x_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(stages + (size_t)p.S * p.stage_bytes);
-    uint64_t* empty = full + p.S;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int ks = blockIdx.y;
-    const int k0 = ks * p.klen;
-    const int c_begin = (int)((long long)p.total_chunks * blockIdx.x / gridDim.x);
-    const int c_end = (int)((long long)p.total_chunks * (blockIdx.x + 1) / gridDim.x);
-    const int n_local = c_end - c_begin;
-    constexpr bool kAffine = (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED);
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < p.S; ++i) {
-            mbar_init(smem_addr(&full[i]), 1);
-            mbar_init(smem_addr(&empty[i]), 1);
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    // ------------------------------------------------------------ producer
-    if (warp == kConsumerWarps) {
-        if (lane != 0) return;
-        const uint64_t pol = l2_evict_first();
-        const long long q_off = (long long)(k0 / kPass) * q_bytes_per_pass(FMT);
-        const int g_off = kAffine ? (k0 >> p.log2gs) : 0;
-        int issued = 0;
-        bool ok = true;
-        for (int i = 0; i < n_local; ++i) {
-            const int st = i % p.S, use = i / p.S;
-            if (use > 0 && !mbar_wait(smem_addr(&empty[st]), (use - 1) & 1)) {
-                report_error(p.err, DEVERR_WAIT_EMPTY);
-                ok = false;
-                break;
-            }
-            const int cid = c_begin + i;
-            const int wi = cid / p.chunks_per_w;
-            const int row0 = (cid - wi * p.chunks_per_w) * R;
-            const int rows = min(R, p.N - row0);
-            uint8_t* dst = stages + (size_t)st * p.stage_bytes;
-            const uint32_t bar = smem_addr(&full[st]);
-            uint32_t bytes = (uint32_t)(rows * p.q_stride);
-            if (kAffine) bytes += 2u * rows * p.sb_stride;
-            mbar_arrive_expect_tx(bar, bytes);
-            const uint8_t* wsrc = p.w[wi] + (long long)row0 * p.q_row_bytes + q_off;
-            if (p.KS == 1) {
-                bulk_g2s(smem_addr(dst), wsrc, rows * p.q_stride, bar, pol);
-                if (kAffine) {
-                    bulk_g2s(smem_addr(dst + p.sb_off), p.s + (long long)row0 * p.G,
-                             rows * p.sb_stride, bar, pol);
-                    bulk_g2s(smem_addr(dst + p.sb_off + R * p.sb_stride),
-                             p.b + (long long)row0 * p.G, rows * p.sb_stride, bar, pol);
-                }
-            } else {
-                for (int r = 0; r < rows; ++r) {
-                    bulk_g2s(smem_addr(dst + r * p.q_stride), wsrc + r * p.q_row_bytes,
-                             p.q_stride, bar, pol);
-                    if (kAffine) {
-                        const long long go = (long long)(row0 + r) * p.G + g_off;
-                        bulk_g2s(smem_addr(dst + p.sb_off + r * p.sb_stride), p.s + go,
-                                 p.sb_stride, bar, pol);
-                        bulk_g2s(smem_addr(dst + p.sb_off + (R + r) * p.sb_stride), p.b + go,
-                                 p.sb_stride, bar, pol);
-                    }
-                }
-            }
-            issued = i + 1;
-        }
-        if (!ok) {
-            // Wait (bounded) for every stage's most recent copies to land
-            // before this block's shared memory can be released.
-            for (int st = 0; st < p.S && st < issued; ++st) {
-                const int last = st + ((issued - 1 - st) / p.S) * p.S;
-                if (!mbar_wait(smem_addr(&full[st]), (last / p.S) & 1))
-                    report_error(p.err, DEVERR_WAIT_DRAIN);
-            }
-        }
-        return;
-    }
-
-    // ------------------------------------------------------------ consumers
-    for (int idx = threadIdx.x; idx < MT * p.klen; idx += kConsumerThreads) {
-        const int m = idx / p.klen, e = idx - m * p.klen;
-        const float v = (m < p.M) ? p.x[(long long)m * p.K + k0 + e] : 0.0f;
-        xs[x_index<FMT>(m, e, p.passes)] = v;
-    }
-    named_bar_sync(1, kConsumerThreads);
-
-    // Lane-constant parts of the decode.
-    int q4k_j0 = 0;
-    if (FMT == FMT_Q4_K) q4k_j0 = 2 * (lane >> 3);
-
-    for (int i = warp; i < n_local; i += kConsumerWarps) {
-        const int st = i % p.S, use = i / p.S;
-        if (!mbar_wait(smem_addr(&full[st]), use & 1)) {
-            report_error(p.err, DEVERR_WAIT_FULL);
-            return;
-        }
-        const int cid = c_begin + i;
-        const int wi = cid / p.chunks_per_w;
-        const int row0 = (cid - wi * p.chunks_per_w) * R;
-        const int rows = min(R, p.N - row0);
-        const uint8_t* stg = stages + (size_t)st * p.stage_bytes;
-
-        float acc[MT][R];
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
-
-#pragma unroll 1
-        for (int pp = 0; pp < p.passes; ++pp) {
-            float xl[MT][4], xh[MT][4];
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                const float4 a = *reinterpret_cast<const float4*>(
-                    xs + (((m * p.passes + pp) * 2 + 0) * 32 + lane) * 4);
-                const float4 c = *reinterpret_cast<const float4*>(
-                    xs + (((m * p.passes + pp) * 2 + 1) * 32 + lane) * 4);
-                xl[m][0] = a.x; xl[m][1] = a.y; xl[m][2] = a.z; xl[m][3] = a.w;
-                xh[m][0] = c.x; xh[m][1] = c.y; xh[m][2] = c.z; xh[m][3] = c.w;
-            }
-            float sxl[MT], sxh[MT];
-            if (FMT != FMT_Q4_0) {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    sxl[m] = (xl[m][0] + xl[m][1]) + (xl[m][2] + xl[m][3]);
-                    sxh[m] = (xh[m][0] + xh[m][1]) + (xh[m][2] + xh[m][3]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (r >= rows) break;
-                const uint8_t* row = stg + r * p.q_stride;
-                if (FMT == FMT_Q4_0) {
-                    const int bl = pp * 8 + (lane >> 2);
-                    const int off = bl * 18 + 2 + (lane & 3) * 4;
-                    const uint32_t* rw = reinterpret_cast<const uint32_t*>(row);
-                    const uint32_t lo = rw[off >> 2], hi = rw[(off >> 2) + 1];
-                    const uint32_t v = __funnelshift_r(lo, hi, (off & 3) * 8);
-                    const float d =
-                        __half2float(*reinterpret_cast<const __half*>(row + bl * 18));
-                    float f[8];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        f[t] = code_f_minus8((v >> (8 * t)) & 0xF);
-                        f[4 + t] = code_f_minus8((v >> (8 * t + 4)) & 0xF);
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        float s = f[0] * xl[m][0];
-#pragma unroll
-                        for (int t = 1; t < 4; ++t) s = __fmaf_rn(f[t], xl[m][t], s);
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) s = __fmaf_rn(f[4 + t], xh[m][t], s);
-                        acc[m][r] = __fmaf_rn(d, s, acc[m][r]);
-                    }
-                } else if (FMT == FMT_Q4_K) {
-                    const uint8_t* blk = row + pp * 144;
-                    const uint32_t hdr = *reinterpret_cast<const uint32_t*>(blk);
-                    const uint32_t s0 = *reinterpret_cast<const uint32_t*>(blk + 4);
-                    const uint32_t s1 = *reinterpret_cast<const uint32_t*>(blk + 8);
-                    const uint32_t s2 = *reinterpret_cast<const uint32_t*>(blk + 12);
-                    const uint32_t v = *reinterpret_cast<const uint32_t*>(blk + 16 + lane * 4);
-                    int sc0, mn0, sc1, mn1;
-                    q4k_pair(s0, s1, s2, q4k_j0, sc0, mn0);
-                    q4k_pair(s0, s1, s2, q4k_j0 + 1, sc1, mn1);
-                    const float d = __half2float(__ushort_as_half((unsigned short)(hdr & 0xFFFF)));
-                    const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr >> 16)));
-                    const float ds0 = d * (float)sc0, dm0 = dmin * (float)mn0;
-                    const float ds1 = d * (float)sc1, dm1 = dmin * (float)mn1;
-                    float f[8];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        f[t] = code_f((v >> (8 * t)) & 0xF);
-                        f[4 + t] = code_f((v >> (8 * t + 4)) & 0xF);
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        float sl = f[0] * xl[m][0];
-#pragma unroll
-                        for (int t = 1; t < 4; ++t) sl = __fmaf_rn(f[t], xl[m][t], sl);
-                        float sh = f[4] * xh[m][0];
-#pragma unroll
-                        for (int t = 1; t < 4; ++t) sh = __fmaf_rn(f[4 + t], xh[m][t], sh);
-                        float a = acc[m][r];
-                        a = __fmaf_rn(ds0, sl, a);
-                        a = __fmaf_rn(-dm0, sxl[m], a);
-                        a = __fmaf_rn(ds1, sh, a);
-                        a = __fmaf_rn(-dm1, sxh[m], a);
-                        acc[m][r] = a;
-                    }
-                } else {
-                    const float* srow =
-                        reinterpret_cast<const float*>(stg + p.sb_off + r * p.sb_stride);
-                    const float* brow =
-                        reinterpret_cast<const float*>(stg + p.sb_off + (R + r) * p.sb_stride);
-                    const int g = (pp * kPass + lane * 8) >> p.log2gs;
-                    const float sc = srow[g], bi = brow[g];
-                    float f[8];
-                    if (FMT == FMT_AFF_U8) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(row + pp * 256 + lane * 8);
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            f[t] = code_f((v.x >> (8 * t)) & 0xFF);
-                            f[4 + t] = code_f((v.y >> (8 * t)) & 0xFF);
-                        }
-                    } else {
-                        const uint32_t v =
-                            *reinterpret_cast<const uint32_t*>(row + pp * 128 + lane * 4);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = code_f((v >> (4 * e)) & 0xF);
-                    }
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        float s = f[0] * xl[m][0];
-#pragma unroll
-                        for (int t = 1; t < 4; ++t) s = __fmaf_rn(f[t], xl[m][t], s);
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) s = __fmaf_rn(f[4 + t], xh[m][t], s);
-                        float a = __fmaf_rn(sc, s, acc[m][r]);
-                        acc[m][r] = __fmaf_rn(bi, sxl[m] + sxh[m], a);
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
-
-        constexpr int V = MT * R;
-        float vals[V];
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int r = 0; r < R; ++r) vals[m * R + r] = acc[m][r];
-        butterfly<V>(vals, lane);
-        constexpr int kSpan = 32 / V;
-        if ((lane % kSpan) == 0) {
-            const int v = lane / kSpan;
-            const int m = v / R, r = v % R;
-            if (m < p.M && r < rows) {
-                const long long o = (long long)m * p.N + row0 + r;
-                if (p.KS == 1)
-                    p.out[wi][o] = vals[0];
-                else
-                    p.partial[((long long)(ks * p.nw + wi) * p.M) * p.N + o] = vals[0];
-            }
-        }
-    }
-}
 
 // Sum of the KS slice partials in slice order: y = ((p0 + p1) + p2) + ...
 __global__ void splitk_finalize(const float* __restrict__ partial, float* y0, float* y1, int nw,
@@ -492,10 +127,29 @@ __global__ void __launch_bounds__(256) gemv_general_kernel(const KParams p) {
     }
 }
 
+
 // ------------------------------------------------------------------ planning
+constexpr int kMaxStages = 32;
+constexpr long long kXMaxBytes = 128 * 1024;
+
+struct FmtGeo {
+    int UE, unit_bytes, nh;
+    bool sums;
+};
+
+FmtGeo geo(int fmt) {
+    switch (fmt) {
+        case FMT_Q4_0: return {32, 18, 1, false};
+        case FMT_Q4_K: return {64, 36, 2, true};
+        case FMT_AFF_U8: return {32, 32, 1, true};
+        default: return {32, 16, 1, true};
+    }
+}
+
 struct Plan {
-    bool fast;
-    int MT, R, KS, klen, S, stage_bytes, q_stride, sb_stride, sb_off, smem;
+    bool fast, co;
+    int MT, R, GW, W, KS, klen, P, S, stage_bytes, q_stride, sb_stride, sb_off, xs_bytes,
+        xsum_bytes, smem, grid_x, stages_per_w;
 };
 
 int ilog2(int v) {
@@ -506,73 +160,128 @@ int ilog2(int v) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+long long row_bytes(int fmt, long long K) {
+    switch (fmt) {
+        case FMT_Q4_0: return K / 32 * 18;
+        case FMT_Q4_K: return K / 256 * 144;
+        case FMT_AFF_U8: return K;
+        default: return K / 2;
+    }
+}
+
+// (R, GW) pairs compiled for each M bucket (see fast::dispatch).
+struct RG {
+    int R, GW;
+};
+int candidates(int fmt, int MT, RG* out) {
+    int n = 0;
+    auto add = [&](int r, int gw) { out[n++] = {r, gw}; };
+    switch (MT) {
+        case 1: add(1, 2); add(1, 4); add(1, 8); add(2, 2); add(2, 4); add(2, 8); add(4, 2); add(4, 4); break;
+        case 2: add(1, 4); add(1, 8); add(2, 2); add(2, 4); break;
+        case 4:
+            add(1, 4); add(1, 8); add(2, 2); add(2, 4);
+            if (fmt != FMT_Q4_K) { add(4, 1); add(4, 2); }
+            break;
+        default:
+            add(1, 2); add(1, 4); add(1, 8);
+            if (fmt != FMT_Q4_K) { add(2, 2); add(2, 4); }
+            break;
+    }
+    return n;
+}
+
+// Planning of one launch for Mc (<= 8) input rows. Stages are single large
+// TMA copies (bulk copies have a high per-copy cost, so pieces of >= 14 KB are
+// preferred); a stage of SR = R*GW rows is consumed by a group of GW warps.
+// When the shared memory fits in half an SM, two CTAs (this kernel's and the
+// next one's) can be resident together, which lets a programmatically
+// launched successor stream its weights while this one drains.
 Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     Plan pl{};
     pl.fast = false;
     const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
+    const FmtGeo g = geo(a.fmt);
     pl.MT = Mc <= 1 ? 1 : Mc <= 2 ? 2 : Mc <= 4 ? 4 : 8;
-    pl.R = pl.MT <= 2 ? 8 : 4;
-    if (a.K % kPass != 0) return pl;
+    pl.W = pl.MT <= 2 ? 16 : 8;
+    if (a.K % g.UE) return pl;
     for (int i = 0; i < a.nw; ++i)
         if (!aligned16(a.w[i])) return pl;
-    const long long qrow = (long long)(a.K / kPass) * q_bytes_per_pass(a.fmt);
-    if (qrow % 16) return pl;
+    if (row_bytes(a.fmt, a.K) % 16) return pl;
     if (affine) {
-        if (a.gs < 8) return pl;
-        const int G = (int)(a.K / a.gs);
-        if (G % 4 != 0 || !aligned16(a.scales) || !aligned16(a.biases)) return pl;
+        if (a.gs < g.UE) return pl;  // a lane's unit must sit inside one group
+        if ((a.K / a.gs) % 4 != 0 || !aligned16(a.scales) || !aligned16(a.biases)) return pl;
     }
-    // k-slices: x for MT inputs must fit in kXMaxBytes.
+    const int PASS = 32 * g.UE;
+    // k-slices: x (padded to whole passes) and its sums must fit kXMaxBytes.
     int KS = 1;
     for (;; ++KS) {
-        if (KS > 8) return pl;
+        if (KS > 16) return pl;
         if (a.K % KS) continue;
         const long long klen = a.K / KS;
-        if (klen % kPass) continue;
+        if (klen % g.UE) continue;
+        if (KS > 1 && (row_bytes(a.fmt, klen) % 16)) continue;
         if (affine && (klen % a.gs || (klen / a.gs) % 4)) continue;
-        if ((long long)pl.MT * klen * 4 <= (long long)kXMaxBytes) break;
+        const long long P = (klen + PASS - 1) / PASS;
+        const long long xb = (long long)pl.MT * P * PASS * 4 + (g.sums ? pl.MT * P * 32 * g.nh * 4 : 0);
+        if (xb <= kXMaxBytes) break;
     }
     pl.KS = KS;
     pl.klen = (int)(a.K / KS);
-    pl.q_stride = (pl.klen / kPass) * q_bytes_per_pass(a.fmt);
+    pl.P = (pl.klen + PASS - 1) / PASS;
+    pl.q_stride = (int)row_bytes(a.fmt, pl.klen);
     pl.sb_stride = affine ? (pl.klen / a.gs) * 4 : 0;
-    pl.sb_off = pl.R * pl.q_stride;
-    int stage = pl.sb_off + 2 * pl.R * pl.sb_stride + 16;
-    pl.stage_bytes = (stage + 127) & ~127;
-    const int x_bytes = (pl.MT * pl.klen * 4 + 127) & ~127;
-    const int avail = dc.max_smem_optin - x_bytes;
-    int S = avail / (pl.stage_bytes + 16);
-    S = std::min(S, kMaxStages);
-    if (S < 2) return pl;
-    pl.S = S;
-    pl.smem = x_bytes + S * pl.stage_bytes + 2 * S * 8;
+    pl.xs_bytes = pl.MT * pl.P * PASS * 4;
+    pl.xsum_bytes = g.sums ? ((pl.MT * pl.P * 32 * g.nh * 4 + 127) & ~127) : 0;
+
+    const long long rows_total = (long long)a.nw * a.N;
+    const int grid_cap = std::max(1, dc.num_sms / KS);
+    const int co_budget = dc.smem_per_sm / 2 - dc.reserved_smem;  // two CTAs per SM
+    RG cand[16];
+    const int nc = candidates(a.fmt, pl.MT, cand);
+    bool have = false;
+    long long best_key = -1;
+    for (int ci = 0; ci < nc; ++ci) {
+        for (int co = 1; co >= 0; --co) {
+            const int R = cand[ci].R, GW = cand[ci].GW, SR = R * GW, NG = pl.W / GW;
+            const int stage = ((SR * pl.q_stride + 2 * SR * pl.sb_stride + 16) + 127) & ~127;
+            const int budget = co ? co_budget : dc.max_smem_optin;
+            const int avail = budget - pl.xs_bytes - pl.xsum_bytes;
+            if (avail <= 0) continue;
+            int S = std::min(kMaxStages, avail / (stage + 16));
+            if (S < 2) continue;
+            if (S >= NG) S = NG * std::min(S / NG, 2);
+            const long long spw = (a.N + SR - 1) / SR;
+            const long long stages_total = spw * a.nw;
+            const int grid = (int)std::min<long long>(stages_total, grid_cap);
+            const double per_cta = (double)stages_total / grid;
+            const int busy_groups = (int)std::min<double>(std::min(NG, S), std::ceil(per_cta));
+            const int busy_warps = busy_groups * GW;
+            // Lexicographic preference: most warps busy (>= 3/4 of them), then
+            // co-residency, then large copies, then row reuse of x, then warps.
+            const long long key = ((long long)(busy_warps * 4 >= pl.W * 3) << 40) |
+                                  ((long long)co << 36) | ((long long)(stage >= 14 * 1024) << 32) |
+                                  ((long long)R << 24) | ((long long)busy_warps << 16) |
+                                  (long long)(64 - S);
+            if (key > best_key) {
+                best_key = key;
+                have = true;
+                pl.R = R;
+                pl.GW = GW;
+                pl.S = S;
+                pl.co = co != 0;
+                pl.stage_bytes = stage;
+                pl.sb_off = SR * pl.q_stride;
+                pl.grid_x = grid;
+                pl.stages_per_w = (int)spw;
+            }
+        }
+    }
+    if (!have) return pl;
+    (void)rows_total;
+    pl.smem = pl.xs_bytes + pl.xsum_bytes + pl.S * pl.stage_bytes + 2 * pl.S * 8;
     pl.fast = true;
     return pl;
-}
-
-template <int FMT, int MT, int R>
-int launch_fast(const DevCtx& dc, const KParams& kp, int grid_x, int smem, cudaStream_t s) {
-    auto kern = gemv_kernel<FMT, MT, R>;
-    static int configured_dev[64] = {0};  // smem opt-in done per device (+1 tag)
-    if (dc.device >= 0 && dc.device < 64 && configured_dev[dc.device] < smem) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dc.max_smem_optin);
-        if (e != cudaSuccess) return cuda_fail(e);
-        configured_dev[dc.device] = dc.max_smem_optin;
-    }
-    kern<<<dim3(grid_x, kp.KS), kThreads, smem, s>>>(kp);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? QG_OK : cuda_fail(e);
-}
-
-template <int FMT>
-int dispatch_fast(const DevCtx& dc, const KParams& kp, const Plan& pl, int grid_x, cudaStream_t s) {
-    switch (pl.MT) {
-        case 1: return launch_fast<FMT, 1, 8>(dc, kp, grid_x, pl.smem, s);
-        case 2: return launch_fast<FMT, 2, 8>(dc, kp, grid_x, pl.smem, s);
-        case 4: return launch_fast<FMT, 4, 4>(dc, kp, grid_x, pl.smem, s);
-        default: return launch_fast<FMT, 8, 4>(dc, kp, grid_x, pl.smem, s);
-    }
 }
 
 template <int FMT>
@@ -584,28 +293,13 @@ int launch_general(const DevCtx& dc, const KParams& kp, cudaStream_t s) {
     return e == cudaSuccess ? QG_OK : cuda_fail(e);
 }
 
-KParams base_params(const DevCtx& dc, const GemvArgs& a) {
-    KParams kp{};
-    kp.w[0] = a.w[0];
-    kp.w[1] = a.nw > 1 ? a.w[1] : a.w[0];
-    kp.s = a.scales;
-    kp.b = a.biases;
-    kp.N = (int)a.N;
-    kp.K = (int)a.K;
-    kp.nw = a.nw;
-    kp.log2gs = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED) ? ilog2(a.gs) : 0;
-    kp.G = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED) ? (int)(a.K / a.gs) : 0;
-    switch (a.fmt) {
-        case FMT_Q4_0: kp.q_row_bytes = a.K / 32 * 18; break;
-        case FMT_Q4_K: kp.q_row_bytes = a.K / 256 * 144; break;
-        case FMT_AFF_U8: kp.q_row_bytes = a.K; break;
-        default: kp.q_row_bytes = a.K / 2; break;
-    }
-    kp.err = dc.err;
-    return kp;
-}
-
 }  // namespace
+
+int fast_launch_q4_0(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
+int fast_launch_q4_k(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
+int fast_launch_aff_u8(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
+int fast_launch_aff_packed(const DevCtx&, const fast::Params&, int, int, int, int, int, bool,
+                           cudaStream_t);
 
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a) {
     size_t worst = 0;
@@ -619,16 +313,30 @@ size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a) {
 }
 
 int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+    const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
     for (long long m0 = 0; m0 < a.M; m0 += 8) {
         const int Mc = (int)std::min<long long>(8, a.M - m0);
-        KParams kp = base_params(dc, a);
-        kp.M = Mc;
-        kp.x = a.x + m0 * a.K;
-        kp.out[0] = a.y[0] + m0 * a.N;
-        kp.out[1] = (a.nw > 1 ? a.y[1] : a.y[0]) + m0 * a.N;
+        const float* x = a.x + m0 * a.K;
+        float* y0 = a.y[0] + m0 * a.N;
+        float* y1 = (a.nw > 1 ? a.y[1] : a.y[0]) + m0 * a.N;
         const Plan pl = make_plan(dc, a, Mc);
         int rc;
         if (!pl.fast) {
+            KParams kp{};
+            kp.w[0] = a.w[0];
+            kp.w[1] = a.nw > 1 ? a.w[1] : a.w[0];
+            kp.out[0] = y0;
+            kp.out[1] = y1;
+            kp.x = x;
+            kp.s = a.scales;
+            kp.b = a.biases;
+            kp.M = Mc;
+            kp.N = (int)a.N;
+            kp.K = (int)a.K;
+            kp.nw = a.nw;
+            kp.log2gs = affine ? ilog2(a.gs) : 0;
+            kp.G = affine ? (int)(a.K / a.gs) : 0;
+            kp.q_row_bytes = row_bytes(a.fmt, a.K);
             switch (a.fmt) {
                 case FMT_Q4_0: rc = launch_general<FMT_Q4_0>(dc, kp, s); break;
                 case FMT_Q4_K: rc = launch_general<FMT_Q4_K>(dc, kp, s); break;
@@ -638,34 +346,61 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
             if (rc != QG_OK) return rc;
             continue;
         }
-        kp.KS = pl.KS;
+        fast::Params kp{};
+        kp.w[0] = a.w[0];
+        kp.w[1] = a.nw > 1 ? a.w[1] : a.w[0];
+        kp.out[0] = y0;
+        kp.out[1] = y1;
+        kp.x = x;
+        kp.s = a.scales;
+        kp.b = a.biases;
+        kp.M = Mc;
+        kp.N = (int)a.N;
+        kp.K = (int)a.K;
+        kp.log2gs = affine ? ilog2(a.gs) : 0;
+        kp.nw = a.nw;
         kp.klen = pl.klen;
-        kp.passes = pl.klen / kPass;
-        kp.chunks_per_w = (int)((a.N + pl.R - 1) / pl.R);
-        kp.total_chunks = kp.chunks_per_w * a.nw;
+        kp.P = pl.P;
+        kp.units = pl.klen / geo(a.fmt).UE;
+        kp.chunks_per_w = pl.stages_per_w;
+        kp.total_chunks = pl.stages_per_w * a.nw;
         kp.S = pl.S;
         kp.stage_bytes = pl.stage_bytes;
         kp.q_stride = pl.q_stride;
         kp.sb_stride = pl.sb_stride;
         kp.sb_off = pl.sb_off;
+        kp.q_row_bytes = row_bytes(a.fmt, a.K);
+        kp.G = affine ? (int)(a.K / a.gs) : 0;
+        kp.KS = pl.KS;
+        kp.xs_bytes = pl.xs_bytes;
+        kp.xsum_bytes = pl.xsum_bytes;
+        kp.magic = 0x4B000000u;
+        kp.err = dc.err;
         if (pl.KS > 1) {
             const size_t need = (size_t)pl.KS * a.nw * Mc * (size_t)a.N * sizeof(float);
             if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE;
             kp.partial = static_cast<float*>(ws);
         }
-        const int grid_x = std::max(1, std::min(kp.total_chunks, dc.num_sms / pl.KS));
+        const bool pdl = launch_option(QG_OPT_PDL) != 0;
         switch (a.fmt) {
-            case FMT_Q4_0: rc = dispatch_fast<FMT_Q4_0>(dc, kp, pl, grid_x, s); break;
-            case FMT_Q4_K: rc = dispatch_fast<FMT_Q4_K>(dc, kp, pl, grid_x, s); break;
-            case FMT_AFF_U8: rc = dispatch_fast<FMT_AFF_U8>(dc, kp, pl, grid_x, s); break;
-            default: rc = dispatch_fast<FMT_AFF_PACKED>(dc, kp, pl, grid_x, s); break;
+            case FMT_Q4_0:
+                rc = fast_launch_q4_0(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                break;
+            case FMT_Q4_K:
+                rc = fast_launch_q4_k(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                break;
+            case FMT_AFF_U8:
+                rc = fast_launch_aff_u8(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                break;
+            default:
+                rc = fast_launch_aff_packed(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                break;
         }
         if (rc != QG_OK) return rc;
         if (pl.KS > 1) {
             const long long MN = (long long)Mc * a.N;
             const long long blocks = std::min<long long>((a.nw * MN + 255) / 256, dc.num_sms * 8);
-            splitk_finalize<<<(int)blocks, 256, 0, s>>>(kp.partial, kp.out[0], kp.out[1], a.nw,
-                                                         pl.KS, MN);
+            splitk_finalize<<<(int)blocks, 256, 0, s>>>(kp.partial, y0, y1, a.nw, pl.KS, MN);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return cuda_fail(e);
         }

@@ -1,0 +1,707 @@
+// The fast GEMV kernel template (16-byte aligned weight rows), included by
+// one translation unit per weight format.
+//
+// Pages: fused_dual_proj_q4_0.rs (mlx-native 0.9.1), q4_k_gemv_v2.rs
+// (ferrum-kernels 0.7.7) and qmm_affine.rs (mlx-native 0.21.1) define the
+// operations; their Metal kernels are not reused. Design for sm_103a:
+//
+//  * One persistent CTA per SM: W consumer warps + 1 producer warp. CTAs take
+//    contiguous, balanced ranges of row chunks (R consecutive rows of one
+//    weight matrix; the dual projection is the row list of W_a then W_b).
+//  * The producer lane streams each chunk's bytes (codes, and for the affine
+//    format the chunk's scales and biases) from HBM into a ring of shared
+//    memory stages with 1-D TMA bulk copies completing on mbarriers, with an
+//    evict-first L2 policy. A whole SM's share of the weights can be in flight
+//    at once without occupying registers.
+//  * x (one k-slice of it) is staged once per CTA in shared memory: permuted so
+//    that every lane's inputs for a pass are consecutive float4 (conflict-free)
+//    and pre-multiplied by a power of two per element (see below). Per-unit
+//    sums of the unscaled x are kept beside it for the formats with an offset
+//    term (Q4_K min, affine bias).
+//  * Stage ownership: chunk i of a CTA lands in stage i % S, and stage st is
+//    always consumed by warp st % W, so every stage's uses are awaited in order.
+//  * Lane <-> unit: each lane owns one unit of UE consecutive weights of a row
+//    (a Q4_0 block of 32, half a Q4_K super-block of 64 = two sub-blocks, 32
+//    affine codes), so per-block scales are read once per 32/64 weights. A warp
+//    covers a pass of 32 units and walks the R rows of its chunk.
+//  * Decode: a nibble at bit 4p of a 32-bit word becomes the exact float
+//    2^23 + q * 2^(4p) with one LOP3 ((word & mask) | 0x4B000000) for bit
+//    positions up to 19; the three nibbles above bit 19 use the word shifted
+//    right by 12. One packed f32x2 subtraction of (2^23 + bias * 2^(4p)) leaves
+//    2^(4p) * (q - bias) exactly. The matching x was pre-multiplied by
+//    2^-(4p), so each product equals (q - bias) * x exactly before its single
+//    rounding in the packed f32x2 FMA (exact for |x| >= 2^-110; smaller
+//    magnitudes could lose bits to subnormal rounding). Bytes (one affine code
+//    per byte) go through PRMT into 2^23 + q with no scaling.
+//  * Partial sums of the R*M outputs are reduced across the warp with a
+//    transposing butterfly and written once.
+//
+// Every output's arithmetic depends only on (format, M bucket, K slicing),
+// never on the CTA, warp, chunk size or matrix that produced it: the dual
+// projection is bitwise equal to two single projections, and packed affine
+// codes give bitwise the same y as one code per byte.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "qg_internal.cuh"
+
+namespace qg {
+namespace fast {
+
+// ------------------------------------------------------------ format traits
+template <int FMT> struct Fmt;
+
+template <> struct Fmt<FMT_Q4_0> {
+    static constexpr int UE = 32;            // weights per lane unit (one block)
+    static constexpr int WORDS = 4;          // 8-weight words per unit
+    static constexpr int UNIT_BYTES = 18;
+    static constexpr bool kSums = false;
+    static constexpr int NH = 1;
+    static constexpr float kBias = 8.0f;
+};
+template <> struct Fmt<FMT_Q4_K> {
+    static constexpr int UE = 64;            // one 32-byte nibble chunk: sub-blocks 2c, 2c+1
+    static constexpr int WORDS = 8;
+    static constexpr int UNIT_BYTES = 36;    // 144 bytes per 4 units
+    static constexpr bool kSums = true;
+    static constexpr int NH = 2;
+    static constexpr float kBias = 0.0f;
+};
+template <> struct Fmt<FMT_AFF_U8> {
+    static constexpr int UE = 32;
+    static constexpr int WORDS = 4;
+    static constexpr int UNIT_BYTES = 32;
+    static constexpr bool kSums = true;
+    static constexpr int NH = 1;
+    static constexpr float kBias = 0.0f;
+};
+template <> struct Fmt<FMT_AFF_PACKED> {
+    static constexpr int UE = 32;
+    static constexpr int WORDS = 4;
+    static constexpr int UNIT_BYTES = 16;
+    static constexpr bool kSums = true;
+    static constexpr int NH = 1;
+    static constexpr float kBias = 0.0f;
+};
+
+// log2 of the scale 2^s carried by the decoded value of element j of a unit
+// (and removed from x at staging time).
+template <int FMT>
+__host__ __device__ __forceinline__ int elem_shift(int j) {
+    if (FMT == FMT_AFF_U8) return 0;
+    if (FMT == FMT_AFF_PACKED) {
+        const int e = j & 7;  // nibble e of the word holding elements 8w..8w+7
+        return e <= 4 ? 4 * e : 4 * (e - 3);
+    }
+    // Q4_0 (32 = 16 low + 16 high) and Q4_K (64 = 32 low + 32 high): byte t of
+    // a word holds a low-half element in bits 8t..8t+3 and a high-half element
+    // in bits 8t+4..8t+7.
+    const int half = (FMT == FMT_Q4_0) ? 16 : 32;
+    const int t = j & 3;
+    const int p = 2 * t + (j >= half ? 1 : 0);  // nibble position in the word
+    return p <= 4 ? 4 * p : 4 * (p - 3);
+}
+
+// Programmatic dependent launch: let the next kernel on the stream launch /
+// wait until the preceding kernel's memory operations are visible. Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Per-kernel parameters (by value).
+struct Params {
+    const uint8_t* w[2];
+    float* out[2];
+    float* partial;
+    const float* x;
+    const float* s;
+    const float* b;
+    int M, N, K;
+    int log2gs;
+    int nw;
+    int klen, P, units;        // k-slice length, passes, units per row slice
+    int chunks_per_w, total_chunks;
+    int S, stage_bytes;
+    int q_stride, sb_stride, sb_off;
+    long long q_row_bytes;
+    int G;
+    int KS;
+    int xs_bytes, xsum_bytes;
+    uint32_t magic;            // 0x4B000000, passed in so it stays in a register
+    unsigned* err;
+};
+
+// 2^23 + bias * 2^s as the constant removed by the packed subtraction.
+__device__ __forceinline__ float magic_sub(float bias, int s) {
+    return 8388608.0f + bias * (float)(1 << s);
+}
+
+// (v & MASK) | mg in one LOP3 (mg arrives in a register so that the mask can
+// be the instruction's immediate).
+template <uint32_t MASK>
+__device__ __forceinline__ float and_or(uint32_t v, uint32_t mg) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "n"(MASK), "r"(mg));
+    return __uint_as_float(d);
+}
+
+// Four packed pairs of exact values 2^s * (q - bias) from one word of eight
+// nibbles; pair order matches x chunks A (.xy, .zw) then B (.xy, .zw).
+// mg = 0x4B000000 (the exponent of 2^23); c[i] = the four constant pairs.
+template <int FMT>
+__device__ __forceinline__ void decode_nibbles(uint32_t v, uint32_t mg, const float2 (&c)[4],
+                                               float2 (&f)[4]) {
+    const uint32_t v2 = v >> 12;
+    const float n0 = and_or<0x0000Fu>(v, mg);   // nibble 0, 2^0
+    const float n1 = and_or<0x000F0u>(v, mg);   // nibble 1, 2^4
+    const float n2 = and_or<0x00F00u>(v, mg);   // nibble 2, 2^8
+    const float n3 = and_or<0x0F000u>(v, mg);   // nibble 3, 2^12
+    const float n4 = and_or<0xF0000u>(v, mg);   // nibble 4, 2^16
+    const float n5 = and_or<0x00F00u>(v2, mg);  // nibble 5, 2^8
+    const float n6 = and_or<0x0F000u>(v2, mg);  // nibble 6, 2^12
+    const float n7 = and_or<0xF0000u>(v2, mg);  // nibble 7, 2^16
+    if (FMT == FMT_AFF_PACKED) {
+        // element e = nibble e: pairs (0,1) (2,3) (4,5) (6,7)
+        f[0] = __fadd2_rn(make_float2(n0, n1), c[0]);
+        f[1] = __fadd2_rn(make_float2(n2, n3), c[1]);
+        f[2] = __fadd2_rn(make_float2(n4, n5), c[2]);
+        f[3] = __fadd2_rn(make_float2(n6, n7), c[3]);
+    } else {
+        // low-half elements t = 0..3 are nibbles 0,2,4,6; high-half 1,3,5,7
+        f[0] = __fadd2_rn(make_float2(n0, n2), c[0]);
+        f[1] = __fadd2_rn(make_float2(n4, n6), c[1]);
+        f[2] = __fadd2_rn(make_float2(n1, n3), c[2]);
+        f[3] = __fadd2_rn(make_float2(n5, n7), c[3]);
+    }
+}
+
+// The constant pairs -(2^23 + bias * 2^s) matching decode_nibbles' pairs.
+template <int FMT>
+__device__ __forceinline__ void decode_consts(float2 (&c)[4]) {
+    const float b = Fmt<FMT>::kBias;
+    if (FMT == FMT_AFF_PACKED) {
+        c[0] = make_float2(-magic_sub(b, 0), -magic_sub(b, 4));
+        c[1] = make_float2(-magic_sub(b, 8), -magic_sub(b, 12));
+        c[2] = make_float2(-magic_sub(b, 16), -magic_sub(b, 8));
+        c[3] = make_float2(-magic_sub(b, 12), -magic_sub(b, 16));
+    } else {
+        c[0] = make_float2(-magic_sub(b, 0), -magic_sub(b, 8));
+        c[1] = make_float2(-magic_sub(b, 16), -magic_sub(b, 12));
+        c[2] = make_float2(-magic_sub(b, 4), -magic_sub(b, 12));
+        c[3] = make_float2(-magic_sub(b, 8), -magic_sub(b, 16));
+    }
+}
+
+// Eight bytes (two words) -> four pairs of exact code values, element order.
+__device__ __forceinline__ void decode_bytes(uint32_t v0, uint32_t v1, uint32_t MG, float2 (&f)[4]) {
+    const float2 c = make_float2(-8388608.0f, -8388608.0f);
+    f[0] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(v0, MG, 0x7540)),
+                                  __uint_as_float(__byte_perm(v0, MG, 0x7541))), c);
+    f[1] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(v0, MG, 0x7542)),
+                                  __uint_as_float(__byte_perm(v0, MG, 0x7543))), c);
+    f[2] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(v1, MG, 0x7540)),
+                                  __uint_as_float(__byte_perm(v1, MG, 0x7541))), c);
+    f[3] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(v1, MG, 0x7542)),
+                                  __uint_as_float(__byte_perm(v1, MG, 0x7543))), c);
+}
+
+// s += f . (xa, xb) as four packed FMAs in a fixed order.
+__device__ __forceinline__ float2 dot8(const float2 (&f)[4], const float4& xa, const float4& xb,
+                                       float2 s) {
+    s = __ffma2_rn(f[0], make_float2(xa.x, xa.y), s);
+    s = __ffma2_rn(f[1], make_float2(xa.z, xa.w), s);
+    s = __ffma2_rn(f[2], make_float2(xb.x, xb.y), s);
+    s = __ffma2_rn(f[3], make_float2(xb.z, xb.w), s);
+    return s;
+}
+
+// Which x chunks (of 4 elements within the lane's unit) word w pairs with.
+template <int FMT>
+__device__ __forceinline__ int chunk_a(int w) {
+    return (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED) ? 2 * w : w;
+}
+template <int FMT>
+__device__ __forceinline__ int chunk_b(int w) {
+    return (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED) ? 2 * w + 1
+                                                        : w + Fmt<FMT>::UE / 8;
+}
+
+// Q4_K (scale, min) pair of sub-block j from the 12 packed bytes as 3 words.
+__device__ __forceinline__ void q4k_pair(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc,
+                                         int& mn) {
+    const int sh = 8 * (j & 3);
+    const uint32_t b0 = (s0 >> sh) & 0xFF, b1 = (s1 >> sh) & 0xFF, b2 = (s2 >> sh) & 0xFF;
+    if (j < 4) {
+        sc = b0 & 63;
+        mn = b1 & 63;
+    } else {
+        sc = (b2 & 15) | ((b0 >> 6) << 4);
+        mn = (b2 >> 4) | ((b1 >> 6) << 4);
+    }
+}
+
+// Per-(row, unit) scale data.
+struct UnitScale {
+    float a0, m0, a1, m1;  // Q4_0: a0 = d. Q4_K: d*sc and dmin*m of both halves.
+};                         // affine: a0 = s, m0 = b.
+
+// Warp reduction of V values at once; lane l ends with value l / (32 / V).
+template <int V>
+__device__ __forceinline__ void butterfly(float (&v)[V], int lane) {
+    int cur = V;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (cur > 1) {
+            const int half = cur / 2;
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < half) {
+                    const float send = upper ? v[i] : v[i + half];
+                    const float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            cur = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+}
+
+template <int FMT, int MT, int R, int W, int GW>
+__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params p) {
+    using F = Fmt<FMT>;
+    constexpr int UE = F::UE;
+    constexpr int NCH = UE / 4;       // float4 chunks of x per unit
+    constexpr int PASS = 32 * UE;
+    constexpr bool kAffine = (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED);
+    constexpr int kThreadsC = W * 32;
+    constexpr int SR = R * GW;        // rows per stage
+    constexpr int NG = W / GW;        // warp groups
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    float* xs = reinterpret_cast<float*>(smem);
+    float* xsum = reinterpret_cast<float*>(smem + p.xs_bytes);
+    uint8_t* stages = smem + p.xs_bytes + p.xsum_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(stages + (size_t)p.S * p.stage_bytes);
+    uint64_t* empty = full + p.S;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ks = blockIdx.y;
+    const int k0 = ks * p.klen;
+    const int c_begin = (int)((long long)p.total_chunks * blockIdx.x / gridDim.x);
+    const int c_end = (int)((long long)p.total_chunks * (blockIdx.x + 1) / gridDim.x);
+    const int n_local = c_end - c_begin;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.S; ++i) {
+            mbar_init(smem_addr(&full[i]), 1);
+            mbar_init(smem_addr(&empty[i]), GW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    // Weights, scales and biases are read before griddepcontrol.wait: under
+    // programmatic dependent launch they must not be written by the kernel
+    // that precedes this one on the stream (the documented contract of that
+    // launch mode). Without it the wait is a no-op.
+    if (warp == W) {
+        if (lane != 0) return;
+        const uint64_t pol = l2_evict_first();
+        const long long q_off = (long long)k0 / UE * F::UNIT_BYTES;
+        const int g_off = kAffine ? (k0 >> p.log2gs) : 0;
+        int issued = 0;
+        bool ok = true;
+        for (int i = 0; i < n_local; ++i) {
+            const int st = i % p.S, use = i / p.S;
+            if (use > 0 && !mbar_wait(smem_addr(&empty[st]), (use - 1) & 1)) {
+                report_error(p.err, DEVERR_WAIT_EMPTY);
+                ok = false;
+                break;
+            }
+            const int cid = c_begin + i;
+            const int wi = cid / p.chunks_per_w;
+            const int row0 = (cid - wi * p.chunks_per_w) * SR;
+            const int rows = min(SR, p.N - row0);
+            uint8_t* dst = stages + (size_t)st * p.stage_bytes;
+            const uint32_t bar = smem_addr(&full[st]);
+            uint32_t bytes = (uint32_t)(rows * p.q_stride);
+            if (kAffine) bytes += 2u * rows * p.sb_stride;
+            mbar_arrive_expect_tx(bar, bytes);
+            const uint8_t* wsrc = p.w[wi] + (long long)row0 * p.q_row_bytes + q_off;
+            if (p.KS == 1) {
+                bulk_g2s(smem_addr(dst), wsrc, rows * p.q_stride, bar, pol);
+                if (kAffine) {
+                    bulk_g2s(smem_addr(dst + p.sb_off), p.s + (long long)row0 * p.G,
+                             rows * p.sb_stride, bar, pol);
+                    bulk_g2s(smem_addr(dst + p.sb_off + SR * p.sb_stride),
+                             p.b + (long long)row0 * p.G, rows * p.sb_stride, bar, pol);
+                }
+            } else {
+                for (int r = 0; r < rows; ++r) {
+                    bulk_g2s(smem_addr(dst + r * p.q_stride), wsrc + r * p.q_row_bytes,
+                             p.q_stride, bar, pol);
+                    if (kAffine) {
+                        const long long go = (long long)(row0 + r) * p.G + g_off;
+                        bulk_g2s(smem_addr(dst + p.sb_off + r * p.sb_stride), p.s + go,
+                                 p.sb_stride, bar, pol);
+                        bulk_g2s(smem_addr(dst + p.sb_off + (SR + r) * p.sb_stride), p.b + go,
+                                 p.sb_stride, bar, pol);
+                    }
+                }
+            }
+            issued = i + 1;
+            // Once the first stages are on their way, the next kernel in the
+            // stream may start its own prologue.
+            if (i == min(n_local, p.S) - 1) pdl_launch_dependents();
+        }
+        if (n_local == 0) pdl_launch_dependents();
+        if (!ok) {
+            // Let every stage's latest copies land before shared memory is released.
+            for (int st = 0; st < p.S && st < issued; ++st) {
+                const int last = st + ((issued - 1 - st) / p.S) * p.S;
+                if (!mbar_wait(smem_addr(&full[st]), (last / p.S) & 1))
+                    report_error(p.err, DEVERR_WAIT_DRAIN);
+            }
+        }
+        return;
+    }
+
+    // x and y may be produced / consumed by the preceding kernel.
+    pdl_wait();
+
+    // ------------------------------------------------- stage x (consumers)
+    // Shift-only index math: UE and PASS are powers of two. Every thread
+    // issues 16 float4 loads (over all MT rows) before its first store, so the
+    // prologue costs about one L2 round trip for the common shapes.
+    constexpr int LOG_UE = (UE == 64) ? 6 : 5;
+    constexpr int LOG_PASS = LOG_UE + 5;
+    {
+        const int span = p.P * PASS;
+        const int quads = span >> 2;
+        const bool vec = ((reinterpret_cast<uintptr_t>(p.x) & 15) == 0) && ((p.K & 3) == 0);
+        constexpr int QU = 16 / MT;  // quads per thread per round, for each of the MT rows
+#pragma unroll 1
+        for (int q0 = threadIdx.x; q0 < quads; q0 += QU * kThreadsC) {
+            float4 v[QU][MT];
+#pragma unroll
+            for (int u = 0; u < QU; ++u) {
+                const int e = (q0 + u * kThreadsC) << 2;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (m < p.M && e < p.klen) {
+                        const float* src = p.x + (long long)m * p.K + k0 + e;
+                        if (vec) {
+                            v[u][m] = *reinterpret_cast<const float4*>(src);
+                        } else {
+                            v[u][m].x = src[0];
+                            v[u][m].y = src[1];
+                            v[u][m].z = src[2];
+                            v[u][m].w = src[3];
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < QU; ++u) {
+                const int e = (q0 + u * kThreadsC) << 2;
+                if (e >= span) break;
+                const int pp = e >> LOG_PASS, within = e & (PASS - 1);
+                const int ln = within >> LOG_UE, j = within & (UE - 1);
+                const float s0 = __uint_as_float((uint32_t)(127 - elem_shift<FMT>(j)) << 23);
+                const float s1 = __uint_as_float((uint32_t)(127 - elem_shift<FMT>(j + 1)) << 23);
+                const float s2 = __uint_as_float((uint32_t)(127 - elem_shift<FMT>(j + 2)) << 23);
+                const float s3 = __uint_as_float((uint32_t)(127 - elem_shift<FMT>(j + 3)) << 23);
+                const int off = ((pp * NCH + (j >> 2)) * 32 + ln) * 4;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float4 o = make_float4(v[u][m].x * s0, v[u][m].y * s1, v[u][m].z * s2,
+                                                 v[u][m].w * s3);
+                    *reinterpret_cast<float4*>(xs + m * span + off) = o;
+                }
+            }
+        }
+        if (F::kSums) {
+            // Sums of the unscaled x over each unit half, in natural element
+            // order, read back from the staged copy (the power-of-two scaling
+            // is undone exactly).
+            named_bar_sync(1, kThreadsC);
+            constexpr int HL = UE / F::NH;  // elements per summed half
+            const int per_m = p.P * 32 * F::NH;
+            for (int idx = threadIdx.x; idx < MT * per_m; idx += kThreadsC) {
+                const int m = idx / per_m, r = idx - m * per_m;  // r = (pp * 32 + lane) * NH + h
+                const int h = r % F::NH, ln = (r / F::NH) & 31, pp = r / (F::NH * 32);
+                const float* xsrc = xs + m * span;
+                float sacc = 0.0f;
+#pragma unroll 8
+                for (int jj = 0; jj < HL; ++jj) {
+                    const int j = h * HL + jj;
+                    const float v = xsrc[((pp * NCH + (j >> 2)) * 32 + ln) * 4 + (j & 3)];
+                    sacc += v * __uint_as_float((uint32_t)(127 + elem_shift<FMT>(j)) << 23);
+                }
+                xsum[idx] = sacc;
+            }
+        }
+    }
+    named_bar_sync(1, kThreadsC);
+
+    const float4* xs4 = reinterpret_cast<const float4*>(xs);
+    const uint32_t mg = p.magic;
+    float2 cst[4];
+    if (FMT != FMT_AFF_U8) decode_consts<FMT>(cst);
+
+    // Stage st is consumed only by warp group st % NG (see the file comment):
+    // with S a multiple of NG group g takes stages g, g+NG, ...; with S < NG,
+    // group g < S takes g, g+S, ... Each warp of the group takes R of the
+    // stage's SR rows.
+    const int grp = warp / GW, gw = warp - grp * GW;
+    const int stride = (p.S >= NG) ? NG : p.S;
+    int st = grp, use = 0;
+    for (int i = grp; i < n_local && grp < stride; i += stride) {
+        if (!mbar_wait(smem_addr(&full[st]), use & 1)) {
+            report_error(p.err, DEVERR_WAIT_FULL);
+            return;
+        }
+        const int cid = c_begin + i;
+        const int wi = cid / p.chunks_per_w;
+        const int row0 = (cid - wi * p.chunks_per_w) * SR + gw * R;
+        const int rows = min(R, p.N - row0);   // may be <= 0 in a ragged last stage
+        const uint8_t* stg = stages + (size_t)st * p.stage_bytes;
+        // Rows past the end of a matrix are computed from stale stage bytes and
+        // never written.
+        const uint8_t* rowp[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) rowp[r] = stg + (gw * R + r) * p.q_stride;
+
+        float acc[MT][R];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
+
+        if (rows > 0) {
+#pragma unroll 1
+        for (int pp = 0; pp < p.P; ++pp) {
+            const int u = pp * 32 + lane;           // unit index within the row slice
+            const bool valid = u < p.units;
+            const int uc = valid ? u : 0;           // clamp for address math
+            const int ub = uc * F::UNIT_BYTES;      // unit's byte offset in a row
+            const float4* xp = xs4 + pp * NCH * 32 + lane;
+
+            // Per-row unit scales (and, for Q4_0, the 20-byte block window).
+            UnitScale us[R];
+            uint32_t win[R][5];
+            uint32_t qsh = 0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (FMT == FMT_Q4_0) {
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp[r] + (ub & ~3));
+#pragma unroll
+                    for (int q = 0; q < 5; ++q) win[r][q] = wp[q];
+                    const uint32_t sh = (uint32_t)(ub & 2) * 8u;  // 0 or 16
+                    qsh = 16u + sh;
+                    const uint32_t dbits = __funnelshift_r(win[r][0], win[r][1], sh) & 0xFFFFu;
+                    us[r].a0 = __half2float(__ushort_as_half((unsigned short)dbits));
+                } else if (FMT == FMT_Q4_K) {
+                    const int sbo = (uc >> 2) * 144, c = uc & 3;
+                    const uint4 h = *reinterpret_cast<const uint4*>(rowp[r] + sbo);
+                    int sc0, mn0, sc1, mn1;
+                    q4k_pair(h.y, h.z, h.w, 2 * c, sc0, mn0);
+                    q4k_pair(h.y, h.z, h.w, 2 * c + 1, sc1, mn1);
+                    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+                    const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                    us[r].a0 = d * (float)sc0;
+                    us[r].m0 = dm * (float)mn0;
+                    us[r].a1 = d * (float)sc1;
+                    us[r].m1 = dm * (float)mn1;
+                } else {
+                    const int g = (uc * UE) >> p.log2gs;
+                    const int sr = gw * R + r;
+                    us[r].a0 = reinterpret_cast<const float*>(stg + p.sb_off + sr * p.sb_stride)[g];
+                    us[r].m0 =
+                        reinterpret_cast<const float*>(stg + p.sb_off + (SR + sr) * p.sb_stride)[g];
+                }
+            }
+            // Byte offset of the unit's nibble words inside a row (Q4_K, affine).
+            const int qo = (FMT == FMT_Q4_K) ? (uc >> 2) * 144 + 16 + 32 * (uc & 3) : ub;
+
+            // Unscaled x sums of the lane's unit halves, per input row.
+            float sx0[MT], sx1[MT];
+            if (F::kSums) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float* xsp = xsum + ((m * p.P + pp) * 32 + lane) * F::NH;
+                    sx0[m] = xsp[0];
+                    sx1[m] = (F::NH > 1) ? xsp[F::NH - 1] : 0.0f;
+                }
+            }
+
+            // Packed partial sums per (m, r); Q4_K keeps its two halves apart.
+            float2 s_lo[MT][R], s_hi[MT][R];
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    s_lo[m][r] = make_float2(0.0f, 0.0f);
+                    s_hi[m][r] = make_float2(0.0f, 0.0f);
+                }
+
+#pragma unroll
+            for (int w = 0; w < F::WORDS; ++w) {
+                float4 xa[MT], xb[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    xa[m] = xp[(m * p.P * NCH + chunk_a<FMT>(w)) * 32];
+                    xb[m] = xp[(m * p.P * NCH + chunk_b<FMT>(w)) * 32];
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float2 f[4];
+                    if (FMT == FMT_Q4_0) {
+                        decode_nibbles<FMT>(__funnelshift_rc(win[r][w], win[r][w + 1], qsh), mg,
+                                            cst, f);
+                    } else if (FMT == FMT_Q4_K || FMT == FMT_AFF_PACKED) {
+                        const uint32_t v = *reinterpret_cast<const uint32_t*>(rowp[r] + qo + 4 * w);
+                        decode_nibbles<FMT>(v, mg, cst, f);
+                    } else {
+                        const uint2 v = *reinterpret_cast<const uint2*>(rowp[r] + qo + 8 * w);
+                        decode_bytes(v.x, v.y, mg, f);
+                    }
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (FMT == FMT_Q4_K) {
+                            s_lo[m][r] = __ffma2_rn(f[0], make_float2(xa[m].x, xa[m].y), s_lo[m][r]);
+                            s_lo[m][r] = __ffma2_rn(f[1], make_float2(xa[m].z, xa[m].w), s_lo[m][r]);
+                            s_hi[m][r] = __ffma2_rn(f[2], make_float2(xb[m].x, xb[m].y), s_hi[m][r]);
+                            s_hi[m][r] = __ffma2_rn(f[3], make_float2(xb[m].z, xb[m].w), s_hi[m][r]);
+                        } else {
+                            s_lo[m][r] = dot8(f, xa[m], xb[m], s_lo[m][r]);
+                        }
+                    }
+                }
+            }
+
+            // Apply the unit scales once per (row, unit); invalid lanes add 0.
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float a = acc[m][r];
+                    if (FMT == FMT_Q4_0) {
+                        a = __fmaf_rn(us[r].a0, s_lo[m][r].x + s_lo[m][r].y, a);
+                    } else if (FMT == FMT_Q4_K) {
+                        a = __fmaf_rn(us[r].a0, s_lo[m][r].x + s_lo[m][r].y, a);
+                        a = __fmaf_rn(-us[r].m0, sx0[m], a);
+                        a = __fmaf_rn(us[r].a1, s_hi[m][r].x + s_hi[m][r].y, a);
+                        a = __fmaf_rn(-us[r].m1, sx1[m], a);
+                    } else {
+                        a = __fmaf_rn(us[r].a0, s_lo[m][r].x + s_lo[m][r].y, a);
+                        a = __fmaf_rn(us[r].m0, sx0[m], a);
+                    }
+                    acc[m][r] = valid ? a : acc[m][r];
+                }
+            }
+        }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+        st += stride;
+        if (st >= p.S) {
+            st -= p.S;
+            ++use;
+        }
+
+        constexpr int V = MT * R;
+        float vals[V];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < R; ++r) vals[m * R + r] = acc[m][r];
+        butterfly<V>(vals, lane);
+        constexpr int kSpan = 32 / V;
+        if ((lane % kSpan) == 0) {
+            const int v = lane / kSpan;
+            const int m = v / R, r = v % R;
+            if (m < p.M && r < rows) {
+                const long long o = (long long)m * p.N + row0 + r;
+                if (p.KS == 1)
+                    p.out[wi][o] = vals[0];
+                else
+                    p.partial[((long long)(ks * p.nw + wi) * p.M) * p.N + o] = vals[0];
+            }
+        }
+    }
+}
+
+// Launch helper used by the per-format translation units. With pdl set the
+// kernel is launched with programmatic stream serialization, so that it can
+// start (and stream its weights) while the previous kernel drains.
+template <int FMT, int MT, int R, int W, int GW>
+int launch(const DevCtx& dc, const Params& kp, int grid_x, int smem, bool pdl, cudaStream_t s) {
+    auto kern = gemv_fast_kernel<FMT, MT, R, W, GW>;
+    static int configured[64] = {0};
+    if (dc.device >= 0 && dc.device < 64 && configured[dc.device] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             dc.max_smem_optin);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured[dc.device] = dc.max_smem_optin;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x, kp.KS);
+    cfg.blockDim = dim3((W + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
+}  // namespace fast
+}  // namespace qg
+
+namespace qg {
+namespace fast {
+
+// (MT, R, GW) -> kernel instantiation. MT <= 2 runs 16 consumer warps in
+// groups of GW, larger M runs 8.
+template <int FMT>
+int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int grid, int smem,
+             bool pdl, cudaStream_t s) {
+#define QG_L(mt, r, w, gw) return launch<FMT, mt, r, w, gw>(dc, kp, grid, smem, pdl, s)
+    switch (MT) {
+        case 1:
+            if (R == 1) { if (GW == 8) QG_L(1, 1, 16, 8); if (GW == 4) QG_L(1, 1, 16, 4); QG_L(1, 1, 16, 2); }
+            if (R == 2) { if (GW == 8) QG_L(1, 2, 16, 8); if (GW == 4) QG_L(1, 2, 16, 4); QG_L(1, 2, 16, 2); }
+            if (GW == 4) QG_L(1, 4, 16, 4);
+            QG_L(1, 4, 16, 2);
+        case 2:
+            if (R == 1) { if (GW == 8) QG_L(2, 1, 16, 8); QG_L(2, 1, 16, 4); }
+            if (GW == 4) QG_L(2, 2, 16, 4);
+            QG_L(2, 2, 16, 2);
+        case 4:
+            if (R == 1) { if (GW == 8) QG_L(4, 1, 8, 8); QG_L(4, 1, 8, 4); }
+            if (R == 2 || FMT == FMT_Q4_K) { if (GW == 4) QG_L(4, 2, 8, 4); QG_L(4, 2, 8, 2); }
+            if constexpr (FMT != FMT_Q4_K) { if (GW == 2) QG_L(4, 4, 8, 2); QG_L(4, 4, 8, 1); }
+            return QG_ERR_UNSUPPORTED;
+        default:
+            if (R == 1 || FMT == FMT_Q4_K) { if (GW == 8) QG_L(8, 1, 8, 8); if (GW == 4) QG_L(8, 1, 8, 4); QG_L(8, 1, 8, 2); }
+            if constexpr (FMT != FMT_Q4_K) { if (GW == 4) QG_L(8, 2, 8, 4); QG_L(8, 2, 8, 2); }
+            return QG_ERR_UNSUPPORTED;
+    }
+#undef QG_L
+}
+
+}  // namespace fast
+}  // namespace qg

@@ -1,0 +1,11 @@
+// Fast GEMV kernels for one weight format (see gemv_fast.cuh).
+#include "gemv_fast.cuh"
+
+namespace qg {
+
+int fast_launch_q4_k(const DevCtx& dc, const fast::Params& kp, int MT, int R, int GW, int grid,
+                   int smem, bool pdl, cudaStream_t s) {
+    return fast::dispatch<FMT_Q4_K>(dc, kp, MT, R, GW, grid, smem, pdl, s);
+}
+
+}  // namespace qg

@@ -4,6 +4,7 @@
 // context, and dispatch to the kernels of gemv.cu and elementwise.cu.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -21,6 +22,7 @@ DevCtx g_ctx[kMaxDevices];
 std::once_flag g_once[kMaxDevices];
 int g_ctx_rc[kMaxDevices];
 thread_local int t_last_cuda_error = 0;
+std::atomic<long long> g_opt_pdl{0};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -28,6 +30,10 @@ int init_ctx(int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaDeviceGetAttribute(&c.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceGetAttribute(&c.reserved_smem, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (e != cudaSuccess) return cuda_fail(e);
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
@@ -126,6 +132,10 @@ int run_gemv(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
 }
 
 }  // namespace
+
+long long launch_option(int option) {
+    return option == QG_OPT_PDL ? g_opt_pdl.load(std::memory_order_relaxed) : 0;
+}
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -286,6 +296,24 @@ int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_size, i
     if (rc) return rc;
     *bytes = gemv_workspace_bytes(*dc, a);
     return QG_OK;
+}
+
+int qg_set_option(int option, int64_t value) {
+    switch (option) {
+        case QG_OPT_PDL:
+            if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
+            g_opt_pdl.store(value, std::memory_order_relaxed);
+            return QG_OK;
+        default: return QG_ERR_INVALID_ARG;
+    }
+}
+
+int qg_get_option(int option, int64_t* value) {
+    if (!value) return QG_ERR_INVALID_ARG;
+    switch (option) {
+        case QG_OPT_PDL: *value = g_opt_pdl.load(std::memory_order_relaxed); return QG_OK;
+        default: return QG_ERR_INVALID_ARG;
+    }
 }
 
 const char* qg_status_string(int status) {

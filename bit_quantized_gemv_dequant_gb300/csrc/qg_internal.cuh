@@ -107,8 +107,13 @@ struct DevCtx {
     int device;
     int num_sms;
     int max_smem_optin;   // bytes of dynamic shared memory a block may opt into
+    int smem_per_sm;      // shared memory per multiprocessor
+    int reserved_smem;    // shared memory the system reserves per block
     unsigned* err;        // device address of this device's error word
 };
+
+// Process-wide launch options set through qg_set_option().
+long long launch_option(int option);
 
 // ----------------------------------------------------------------- launchers
 // GEMV family (gemv.cu). fmt: see GemvFmt. Returns a qg_status.

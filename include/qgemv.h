@@ -145,6 +145,21 @@ QG_API int dequant_affine(const void* q, const float* scales, const float* biase
 QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_size, int packed,
                       size_t* bytes);
 
+/* Process-wide launch options (not a counterpart of anything on the pages;
+ * they select how this library's kernels are launched).
+ *
+ * QG_OPT_PDL (default 0): 1 launches the GEMV/qmm kernels with programmatic
+ * dependent launch. A kernel then starts while the previous kernel on the
+ * stream is still draining and streams its weights right away; it waits for
+ * the previous kernel to complete only before it reads x and writes y. The
+ * caller promises that the weight codes, scales and biases of a call are not
+ * written by the kernel immediately preceding it on the stream (static model
+ * weights satisfy this). Back-to-back decode projections overlap one call's
+ * ramp-up with the previous call's tail this way. */
+enum { QG_OPT_PDL = 1 };
+QG_API int qg_set_option(int option, int64_t value);
+QG_API int qg_get_option(int option, int64_t* value);
+
 /* Human-readable text of a qg_status. Never NULL. */
 QG_API const char* qg_status_string(int status);
 

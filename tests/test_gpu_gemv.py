@@ -193,6 +193,45 @@ def test_affine_equals_dequant_then_matmul():
     assert_parity(y, comp, bound, what="fused vs composed")
 
 
+# ------------------------------------------------- programmatic dependent launch
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_pdl_chain_reads_previous_output(M):
+    """With QG_OPT_PDL a call may start while the previous one drains; it must
+    still see the previous call's y when that y is its x."""
+    N = K = 1024
+    c = synth.q4_0_case(2100 + M, N, K, M, dual=True)
+    wa, wb = to_dev(c["w"]), to_dev(c["w_b"])
+    ck = synth.q4_k_case(2200 + M, N, K, M)
+    wk = to_dev(ck["w"])
+    qg.set_option(qg.QG_OPT_PDL, 1)
+    try:
+        x0 = to_dev(c["x"])
+        ya, yb = qg.qgemv_dual_q4_0(wa, wb, x0, N=N)   # x1 = ya
+        y2 = qg.qgemv_q4_k(wk, ya, N=N)                 # x2 = y2
+        y3 = qg.qgemv_q4_0(wb, y2, N=N)
+        torch.cuda.synchronize()
+    finally:
+        qg.set_option(qg.QG_OPT_PDL, 0)
+    # The oracle replays the chain on the GPU's own intermediate outputs, so
+    # each stage is checked against exactly the input it was given.
+    (ra, ba), _ = oracle.gemv_dual_q4_0(c["w"], c["w_b"], c["x"], M, N, K)
+    assert_parity(ya, ra, ba, what="chain stage 1")
+    r2, b2 = oracle.gemv_q4_k(ck["w"], ya.cpu().numpy(), M, N, K)
+    assert_parity(y2, r2, b2, what="chain stage 2")
+    r3, b3 = oracle.gemv_q4_0(c["w_b"], y2.cpu().numpy(), M, N, K)
+    assert_parity(y3, r3, b3, what="chain stage 3")
+    assert qg.device_error() == 0
+
+
+def test_pdl_option_roundtrip():
+    assert qg.get_option(qg.QG_OPT_PDL) == 0
+    qg.set_option(qg.QG_OPT_PDL, 1)
+    assert qg.get_option(qg.QG_OPT_PDL) == 1
+    qg.set_option(qg.QG_OPT_PDL, 0)
+    with pytest.raises(qg.QGError):
+        qg.set_option(qg.QG_OPT_PDL, 5)
+
+
 # ------------------------------------------------------------- error paths
 def test_invalid_arguments_rejected_before_launch():
     x = torch.zeros((1, 64), device=dev())
