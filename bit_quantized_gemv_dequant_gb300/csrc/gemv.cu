@@ -169,34 +169,26 @@ long long row_bytes(int fmt, long long K) {
     }
 }
 
-// (R, GW) pairs compiled for each M bucket (see fast::dispatch).
-struct RG {
-    int R, GW;
-};
-int candidates(int fmt, int MT, RG* out) {
+// Rows-per-stage options compiled for each M bucket (see fast::dispatch).
+int r_options(int MT, int* out) {
     int n = 0;
-    auto add = [&](int r, int gw) { out[n++] = {r, gw}; };
     switch (MT) {
-        case 1: add(1, 2); add(1, 4); add(1, 8); add(2, 2); add(2, 4); add(2, 8); add(4, 2); add(4, 4); break;
-        case 2: add(1, 4); add(1, 8); add(2, 2); add(2, 4); break;
-        case 4:
-            add(1, 4); add(1, 8); add(2, 2); add(2, 4);
-            if (fmt != FMT_Q4_K) { add(4, 1); add(4, 2); }
-            break;
-        default:
-            add(1, 2); add(1, 4); add(1, 8);
-            if (fmt != FMT_Q4_K) { add(2, 2); add(2, 4); }
-            break;
+        case 1: out[n++] = 2; out[n++] = 4; out[n++] = 8; break;
+        case 2: out[n++] = 2; out[n++] = 4; break;
+        case 4: out[n++] = 2; out[n++] = 4; break;
+        default: out[n++] = 1; out[n++] = 2; out[n++] = 4; break;
     }
     return n;
 }
 
-// Planning of one launch for Mc (<= 8) input rows. Stages are single large
-// TMA copies (bulk copies have a high per-copy cost, so pieces of >= 14 KB are
-// preferred); a stage of SR = R*GW rows is consumed by a group of GW warps.
-// When the shared memory fits in half an SM, two CTAs (this kernel's and the
-// next one's) can be resident together, which lets a programmatically
-// launched successor stream its weights while this one drains.
+// Planning of one launch for Mc (<= 8) input rows. A stage of R rows is one
+// large TMA copy (bulk copies have a high per-copy cost, so pieces of >= 14 KB
+// are preferred) shared by a group of GW warps, which split the k passes; GW
+// depends only on the pass count, never on N or the number of matrices, so
+// the arithmetic of every output is the same for single and dual calls. When
+// the shared memory fits in half an SM, two CTAs (this kernel's and the next
+// one's) can be resident together, which lets a programmatically launched
+// successor stream its weights while this one drains.
 Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     Plan pl{};
     pl.fast = false;
@@ -229,56 +221,59 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     pl.KS = KS;
     pl.klen = (int)(a.K / KS);
     pl.P = (pl.klen + PASS - 1) / PASS;
+    pl.GW = pl.P >= 4 ? 4 : (pl.P >= 2 ? 2 : 1);
     pl.q_stride = (int)row_bytes(a.fmt, pl.klen);
     pl.sb_stride = affine ? (pl.klen / a.gs) * 4 : 0;
     pl.xs_bytes = pl.MT * pl.P * PASS * 4;
-    pl.xsum_bytes = g.sums ? ((pl.MT * pl.P * 32 * g.nh * 4 + 127) & ~127) : 0;
 
-    const long long rows_total = (long long)a.nw * a.N;
+    const int NG = pl.W / pl.GW;
     const int grid_cap = std::max(1, dc.num_sms / KS);
     const int co_budget = dc.smem_per_sm / 2 - dc.reserved_smem;  // two CTAs per SM
-    RG cand[16];
-    const int nc = candidates(a.fmt, pl.MT, cand);
+    int ropt[4];
+    const int nr = r_options(pl.MT, ropt);
     bool have = false;
     long long best_key = -1;
-    for (int ci = 0; ci < nc; ++ci) {
+    for (int ri = 0; ri < nr; ++ri) {
+        const int R = ropt[ri];
+        if (R > fast::max_rows(a.fmt, pl.MT)) continue;
+        const int V = pl.MT * R;
+        const int sums = g.sums ? pl.MT * pl.P * 32 * g.nh : 0;
+        const int xsum_bytes = ((sums + 2 * pl.W * V) * 4 + 127) & ~127;
         for (int co = 1; co >= 0; --co) {
-            const int R = cand[ci].R, GW = cand[ci].GW, SR = R * GW, NG = pl.W / GW;
-            const int stage = ((SR * pl.q_stride + 2 * SR * pl.sb_stride + 16) + 127) & ~127;
+            const int stage = ((R * pl.q_stride + 2 * R * pl.sb_stride + 16) + 127) & ~127;
             const int budget = co ? co_budget : dc.max_smem_optin;
-            const int avail = budget - pl.xs_bytes - pl.xsum_bytes;
+            const int avail = budget - pl.xs_bytes - xsum_bytes;
             if (avail <= 0) continue;
             int S = std::min(kMaxStages, avail / (stage + 16));
             if (S < 2) continue;
             if (S >= NG) S = NG * std::min(S / NG, 2);
-            const long long spw = (a.N + SR - 1) / SR;
+            const long long spw = (a.N + R - 1) / R;
             const long long stages_total = spw * a.nw;
             const int grid = (int)std::min<long long>(stages_total, grid_cap);
             const double per_cta = (double)stages_total / grid;
             const int busy_groups = (int)std::min<double>(std::min(NG, S), std::ceil(per_cta));
-            const int busy_warps = busy_groups * GW;
+            const int busy_warps = busy_groups * pl.GW;
             // Lexicographic preference: most warps busy (>= 3/4 of them), then
             // co-residency, then large copies, then row reuse of x, then warps.
             const long long key = ((long long)(busy_warps * 4 >= pl.W * 3) << 40) |
                                   ((long long)co << 36) | ((long long)(stage >= 14 * 1024) << 32) |
                                   ((long long)R << 24) | ((long long)busy_warps << 16) |
-                                  (long long)(64 - S);
+                                  (long long)S;
             if (key > best_key) {
                 best_key = key;
                 have = true;
                 pl.R = R;
-                pl.GW = GW;
                 pl.S = S;
                 pl.co = co != 0;
                 pl.stage_bytes = stage;
-                pl.sb_off = SR * pl.q_stride;
+                pl.xsum_bytes = xsum_bytes;
+                pl.sb_off = R * pl.q_stride;
                 pl.grid_x = grid;
                 pl.stages_per_w = (int)spw;
             }
         }
     }
     if (!have) return pl;
-    (void)rows_total;
     pl.smem = pl.xs_bytes + pl.xsum_bytes + pl.S * pl.stage_bytes + 2 * pl.S * 8;
     pl.fast = true;
     return pl;

@@ -280,8 +280,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
     constexpr int PASS = 32 * UE;
     constexpr bool kAffine = (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED);
     constexpr int kThreadsC = W * 32;
-    constexpr int SR = R * GW;        // rows per stage
+    constexpr int SR = R;             // rows per stage (all GW warps of a group share them)
     constexpr int NG = W / GW;        // warp groups
+    constexpr int RB = (MT == 1) ? (R < 4 ? R : 4) : (R < 2 ? R : 2);  // row batch
 
     extern __shared__ __align__(128) uint8_t smem[];
     float* xs = reinterpret_cast<float*>(smem);
@@ -457,29 +458,38 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
     const uint32_t mg = p.magic;
     float2 cst[4];
     if (FMT != FMT_AFF_U8) decode_consts<FMT>(cst);
+    // Cross-warp partial sums of a group: [2 (stage parity)][NG][GW][V], kept
+    // in the last red_floats() floats of the x-sum region.
+    constexpr int V = MT * R;
+    float* red = xsum + (p.xsum_bytes >> 2) - 2 * W * V;
 
     // Stage st is consumed only by warp group st % NG (see the file comment):
     // with S a multiple of NG group g takes stages g, g+NG, ...; with S < NG,
-    // group g < S takes g, g+S, ... Each warp of the group takes R of the
-    // stage's SR rows.
+    // group g < S takes g, g+S, ... The GW warps of a group split the passes
+    // of the k-slice (warp gw takes passes gw, gw+GW, ...) for all R rows of
+    // the stage and add their partial sums in warp order.
     const int grp = warp / GW, gw = warp - grp * GW;
     const int stride = (p.S >= NG) ? NG : p.S;
     int st = grp, use = 0;
+    // After a wait gives up the warp keeps stepping through its stages (and
+    // the group's named barriers) without computing, so that no other warp
+    // of the group is left waiting at a barrier.
+    bool dead = false;
     for (int i = grp; i < n_local && grp < stride; i += stride) {
-        if (!mbar_wait(smem_addr(&full[st]), use & 1)) {
+        if (!dead && !mbar_wait(smem_addr(&full[st]), use & 1)) {
             report_error(p.err, DEVERR_WAIT_FULL);
-            return;
+            dead = true;
         }
         const int cid = c_begin + i;
         const int wi = cid / p.chunks_per_w;
-        const int row0 = (cid - wi * p.chunks_per_w) * SR + gw * R;
-        const int rows = min(R, p.N - row0);   // may be <= 0 in a ragged last stage
+        const int row0 = (cid - wi * p.chunks_per_w) * R;
+        const int rows = min(R, p.N - row0);
         const uint8_t* stg = stages + (size_t)st * p.stage_bytes;
-        // Rows past the end of a matrix are computed from stale stage bytes and
-        // never written.
+        // Rows past the end of a matrix (ragged last stage) are computed from
+        // stale stage bytes and never written.
         const uint8_t* rowp[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) rowp[r] = stg + (gw * R + r) * p.q_stride;
+        for (int r = 0; r < R; ++r) rowp[r] = stg + r * p.q_stride;
 
         float acc[MT][R];
 #pragma unroll
@@ -487,51 +497,16 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
 #pragma unroll
             for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
 
-        if (rows > 0) {
 #pragma unroll 1
-        for (int pp = 0; pp < p.P; ++pp) {
+        for (int pp = gw; pp < (dead ? 0 : p.P); pp += GW) {
             const int u = pp * 32 + lane;           // unit index within the row slice
             const bool valid = u < p.units;
             const int uc = valid ? u : 0;           // clamp for address math
             const int ub = uc * F::UNIT_BYTES;      // unit's byte offset in a row
             const float4* xp = xs4 + pp * NCH * 32 + lane;
-
-            // Per-row unit scales (and, for Q4_0, the 20-byte block window).
-            UnitScale us[R];
-            uint32_t win[R][5];
-            uint32_t qsh = 0;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (FMT == FMT_Q4_0) {
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp[r] + (ub & ~3));
-#pragma unroll
-                    for (int q = 0; q < 5; ++q) win[r][q] = wp[q];
-                    const uint32_t sh = (uint32_t)(ub & 2) * 8u;  // 0 or 16
-                    qsh = 16u + sh;
-                    const uint32_t dbits = __funnelshift_r(win[r][0], win[r][1], sh) & 0xFFFFu;
-                    us[r].a0 = __half2float(__ushort_as_half((unsigned short)dbits));
-                } else if (FMT == FMT_Q4_K) {
-                    const int sbo = (uc >> 2) * 144, c = uc & 3;
-                    const uint4 h = *reinterpret_cast<const uint4*>(rowp[r] + sbo);
-                    int sc0, mn0, sc1, mn1;
-                    q4k_pair(h.y, h.z, h.w, 2 * c, sc0, mn0);
-                    q4k_pair(h.y, h.z, h.w, 2 * c + 1, sc1, mn1);
-                    const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
-                    const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-                    us[r].a0 = d * (float)sc0;
-                    us[r].m0 = dm * (float)mn0;
-                    us[r].a1 = d * (float)sc1;
-                    us[r].m1 = dm * (float)mn1;
-                } else {
-                    const int g = (uc * UE) >> p.log2gs;
-                    const int sr = gw * R + r;
-                    us[r].a0 = reinterpret_cast<const float*>(stg + p.sb_off + sr * p.sb_stride)[g];
-                    us[r].m0 =
-                        reinterpret_cast<const float*>(stg + p.sb_off + (SR + sr) * p.sb_stride)[g];
-                }
-            }
             // Byte offset of the unit's nibble words inside a row (Q4_K, affine).
             const int qo = (FMT == FMT_Q4_K) ? (uc >> 2) * 144 + 16 + 32 * (uc & 3) : ub;
+            const uint32_t qsh = 16u + (uint32_t)(ub & 2) * 8u;  // Q4_0: 16 or 32
 
             // Unscaled x sums of the lane's unit halves, per input row.
             float sx0[MT], sx1[MT];
@@ -544,82 +519,115 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                 }
             }
 
-            // Packed partial sums per (m, r); Q4_K keeps its two halves apart.
-            float2 s_lo[MT][R], s_hi[MT][R];
+            // Rows in batches of RB: the batch's block windows / unit scales stay
+            // in registers while each x word is loaded once and used RB times.
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
+            for (int rb0 = 0; rb0 < R; rb0 += RB) {
+                UnitScale us[RB];
+                uint32_t win[RB][5];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    s_lo[m][r] = make_float2(0.0f, 0.0f);
-                    s_hi[m][r] = make_float2(0.0f, 0.0f);
+                for (int b = 0; b < RB; ++b) {
+                    const int r = rb0 + b;
+                    if (FMT == FMT_Q4_0) {
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp[r] + (ub & ~3));
+#pragma unroll
+                        for (int q = 0; q < 5; ++q) win[b][q] = wp[q];
+                        const uint32_t dbits =
+                            __funnelshift_r(win[b][0], win[b][1], qsh - 16u) & 0xFFFFu;
+                        us[b].a0 = __half2float(__ushort_as_half((unsigned short)dbits));
+                    } else if (FMT == FMT_Q4_K) {
+                        const int c = uc & 3;
+                        const uint4 h = *reinterpret_cast<const uint4*>(rowp[r] + (uc >> 2) * 144);
+                        int sc0, mn0, sc1, mn1;
+                        q4k_pair(h.y, h.z, h.w, 2 * c, sc0, mn0);
+                        q4k_pair(h.y, h.z, h.w, 2 * c + 1, sc1, mn1);
+                        const float d =
+                            __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+                        const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                        us[b].a0 = d * (float)sc0;
+                        us[b].m0 = dm * (float)mn0;
+                        us[b].a1 = d * (float)sc1;
+                        us[b].m1 = dm * (float)mn1;
+                    } else {
+                        const int g = (uc * UE) >> p.log2gs;
+                        us[b].a0 =
+                            reinterpret_cast<const float*>(stg + p.sb_off + r * p.sb_stride)[g];
+                        us[b].m0 =
+                            reinterpret_cast<const float*>(stg + p.sb_off + (R + r) * p.sb_stride)[g];
+                    }
                 }
 
+                // Packed partial sums per (m, row); Q4_K keeps its two halves apart.
+                float2 s_lo[MT][RB], s_hi[MT][RB];
 #pragma unroll
-            for (int w = 0; w < F::WORDS; ++w) {
-                float4 xa[MT], xb[MT];
+                for (int m = 0; m < MT; ++m)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    xa[m] = xp[(m * p.P * NCH + chunk_a<FMT>(w)) * 32];
-                    xb[m] = xp[(m * p.P * NCH + chunk_b<FMT>(w)) * 32];
-                }
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float2 f[4];
-                    if (FMT == FMT_Q4_0) {
-                        decode_nibbles<FMT>(__funnelshift_rc(win[r][w], win[r][w + 1], qsh), mg,
-                                            cst, f);
-                    } else if (FMT == FMT_Q4_K || FMT == FMT_AFF_PACKED) {
-                        const uint32_t v = *reinterpret_cast<const uint32_t*>(rowp[r] + qo + 4 * w);
-                        decode_nibbles<FMT>(v, mg, cst, f);
-                    } else {
-                        const uint2 v = *reinterpret_cast<const uint2*>(rowp[r] + qo + 8 * w);
-                        decode_bytes(v.x, v.y, mg, f);
+                    for (int b = 0; b < RB; ++b) {
+                        s_lo[m][b] = make_float2(0.0f, 0.0f);
+                        s_hi[m][b] = make_float2(0.0f, 0.0f);
                     }
 #pragma unroll
+                for (int w = 0; w < F::WORDS; ++w) {
+                    float4 xa[MT], xb[MT];
+#pragma unroll
                     for (int m = 0; m < MT; ++m) {
-                        if (FMT == FMT_Q4_K) {
-                            s_lo[m][r] = __ffma2_rn(f[0], make_float2(xa[m].x, xa[m].y), s_lo[m][r]);
-                            s_lo[m][r] = __ffma2_rn(f[1], make_float2(xa[m].z, xa[m].w), s_lo[m][r]);
-                            s_hi[m][r] = __ffma2_rn(f[2], make_float2(xb[m].x, xb[m].y), s_hi[m][r]);
-                            s_hi[m][r] = __ffma2_rn(f[3], make_float2(xb[m].z, xb[m].w), s_hi[m][r]);
+                        xa[m] = xp[(m * p.P * NCH + chunk_a<FMT>(w)) * 32];
+                        xb[m] = xp[(m * p.P * NCH + chunk_b<FMT>(w)) * 32];
+                    }
+#pragma unroll
+                    for (int b = 0; b < RB; ++b) {
+                        const int r = rb0 + b;
+                        float2 f[4];
+                        if (FMT == FMT_Q4_0) {
+                            decode_nibbles<FMT>(__funnelshift_rc(win[b][w], win[b][w + 1], qsh), mg,
+                                                cst, f);
+                        } else if (FMT == FMT_Q4_K || FMT == FMT_AFF_PACKED) {
+                            const uint32_t v =
+                                *reinterpret_cast<const uint32_t*>(rowp[r] + qo + 4 * w);
+                            decode_nibbles<FMT>(v, mg, cst, f);
                         } else {
-                            s_lo[m][r] = dot8(f, xa[m], xb[m], s_lo[m][r]);
+                            const uint2 v = *reinterpret_cast<const uint2*>(rowp[r] + qo + 8 * w);
+                            decode_bytes(v.x, v.y, mg, f);
+                        }
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            if (FMT == FMT_Q4_K) {
+                                s_lo[m][b] = __ffma2_rn(f[0], make_float2(xa[m].x, xa[m].y), s_lo[m][b]);
+                                s_lo[m][b] = __ffma2_rn(f[1], make_float2(xa[m].z, xa[m].w), s_lo[m][b]);
+                                s_hi[m][b] = __ffma2_rn(f[2], make_float2(xb[m].x, xb[m].y), s_hi[m][b]);
+                                s_hi[m][b] = __ffma2_rn(f[3], make_float2(xb[m].z, xb[m].w), s_hi[m][b]);
+                            } else {
+                                s_lo[m][b] = dot8(f, xa[m], xb[m], s_lo[m][b]);
+                            }
                         }
                     }
                 }
-            }
-
-            // Apply the unit scales once per (row, unit); invalid lanes add 0.
+                // Apply the unit scales once per (row, unit); invalid lanes add 0.
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
+                for (int b = 0; b < RB; ++b) {
+                    const int r = rb0 + b;
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float a = acc[m][r];
-                    if (FMT == FMT_Q4_0) {
-                        a = __fmaf_rn(us[r].a0, s_lo[m][r].x + s_lo[m][r].y, a);
-                    } else if (FMT == FMT_Q4_K) {
-                        a = __fmaf_rn(us[r].a0, s_lo[m][r].x + s_lo[m][r].y, a);
-                        a = __fmaf_rn(-us[r].m0, sx0[m], a);
-                        a = __fmaf_rn(us[r].a1, s_hi[m][r].x + s_hi[m][r].y, a);
-                        a = __fmaf_rn(-us[r].m1, sx1[m], a);
-                    } else {
-                        a = __fmaf_rn(us[r].a0, s_lo[m][r].x + s_lo[m][r].y, a);
-                        a = __fmaf_rn(us[r].m0, sx0[m], a);
+                    for (int m = 0; m < MT; ++m) {
+                        float a = acc[m][r];
+                        if (FMT == FMT_Q4_0) {
+                            a = __fmaf_rn(us[b].a0, s_lo[m][b].x + s_lo[m][b].y, a);
+                        } else if (FMT == FMT_Q4_K) {
+                            a = __fmaf_rn(us[b].a0, s_lo[m][b].x + s_lo[m][b].y, a);
+                            a = __fmaf_rn(-us[b].m0, sx0[m], a);
+                            a = __fmaf_rn(us[b].a1, s_hi[m][b].x + s_hi[m][b].y, a);
+                            a = __fmaf_rn(-us[b].m1, sx1[m], a);
+                        } else {
+                            a = __fmaf_rn(us[b].a0, s_lo[m][b].x + s_lo[m][b].y, a);
+                            a = __fmaf_rn(us[b].m0, sx0[m], a);
+                        }
+                        acc[m][r] = valid ? a : acc[m][r];
                     }
-                    acc[m][r] = valid ? a : acc[m][r];
                 }
             }
         }
-        }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
-        st += stride;
-        if (st >= p.S) {
-            st -= p.S;
-            ++use;
-        }
 
-        constexpr int V = MT * R;
         float vals[V];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -627,16 +635,33 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
             for (int r = 0; r < R; ++r) vals[m * R + r] = acc[m][r];
         butterfly<V>(vals, lane);
         constexpr int kSpan = 32 / V;
-        if ((lane % kSpan) == 0) {
-            const int v = lane / kSpan;
+        const bool holder = (lane % kSpan) == 0;
+        const int v = lane / kSpan;
+        float total = vals[0];
+        if (GW > 1) {
+            float* rb = red + (((use & 1) * NG + grp) * GW) * V;
+            if (holder) rb[gw * V + v] = total;
+            named_bar_sync(2 + grp, GW * 32);
+            if (gw == 0 && holder) {
+                total = rb[v];
+#pragma unroll
+                for (int g2 = 1; g2 < GW; ++g2) total += rb[g2 * V + v];
+            }
+        }
+        if (gw == 0 && holder) {
             const int m = v / R, r = v % R;
             if (m < p.M && r < rows) {
                 const long long o = (long long)m * p.N + row0 + r;
                 if (p.KS == 1)
-                    p.out[wi][o] = vals[0];
+                    p.out[wi][o] = total;
                 else
-                    p.partial[((long long)(ks * p.nw + wi) * p.M) * p.N + o] = vals[0];
+                    p.partial[((long long)(ks * p.nw + wi) * p.M) * p.N + o] = total;
             }
+        }
+        st += stride;
+        if (st >= p.S) {
+            st -= p.S;
+            ++use;
         }
     }
 }
@@ -674,33 +699,49 @@ int launch(const DevCtx& dc, const Params& kp, int grid_x, int smem, bool pdl, c
 namespace qg {
 namespace fast {
 
-// (MT, R, GW) -> kernel instantiation. MT <= 2 runs 16 consumer warps in
-// groups of GW, larger M runs 8.
+// Largest rows-per-stage per (format, M bucket) that compiles without
+// register spills (16 consumer warps cap a thread at 96 registers, 8 at 168).
+__host__ __device__ constexpr int max_rows(int fmt, int MT) {
+    return fmt == FMT_Q4_0   ? (MT == 1 ? 8 : MT == 8 ? 2 : 4)
+           : fmt == FMT_Q4_K ? (MT == 1 ? 4 : MT == 8 ? 1 : 2)
+                             : (MT == 1 ? 8 : 2);
+}
+
+// (MT, R, GW) -> kernel instantiation: R rows per stage, shared by a group of
+// GW warps that split the passes. MT <= 2 runs 16 consumer warps, larger M 8.
+template <int FMT, int MT, int W, int R>
+int dispatch_gw(const DevCtx& dc, const Params& kp, int GW, int grid, int smem, bool pdl,
+                cudaStream_t s) {
+    if constexpr (R > max_rows(FMT, MT)) {
+        return QG_ERR_UNSUPPORTED;
+    } else {
+        switch (GW) {
+            case 1: return launch<FMT, MT, R, W, 1>(dc, kp, grid, smem, pdl, s);
+            case 2: return launch<FMT, MT, R, W, 2>(dc, kp, grid, smem, pdl, s);
+            default: return launch<FMT, MT, R, W, 4>(dc, kp, grid, smem, pdl, s);
+        }
+    }
+}
+
 template <int FMT>
 int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int grid, int smem,
              bool pdl, cudaStream_t s) {
-#define QG_L(mt, r, w, gw) return launch<FMT, mt, r, w, gw>(dc, kp, grid, smem, pdl, s)
     switch (MT) {
         case 1:
-            if (R == 1) { if (GW == 8) QG_L(1, 1, 16, 8); if (GW == 4) QG_L(1, 1, 16, 4); QG_L(1, 1, 16, 2); }
-            if (R == 2) { if (GW == 8) QG_L(1, 2, 16, 8); if (GW == 4) QG_L(1, 2, 16, 4); QG_L(1, 2, 16, 2); }
-            if (GW == 4) QG_L(1, 4, 16, 4);
-            QG_L(1, 4, 16, 2);
+            if (R <= 2) return dispatch_gw<FMT, 1, 16, 2>(dc, kp, GW, grid, smem, pdl, s);
+            if (R == 4) return dispatch_gw<FMT, 1, 16, 4>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 1, 16, 8>(dc, kp, GW, grid, smem, pdl, s);
         case 2:
-            if (R == 1) { if (GW == 8) QG_L(2, 1, 16, 8); QG_L(2, 1, 16, 4); }
-            if (GW == 4) QG_L(2, 2, 16, 4);
-            QG_L(2, 2, 16, 2);
+            if (R <= 2) return dispatch_gw<FMT, 2, 16, 2>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 2, 16, 4>(dc, kp, GW, grid, smem, pdl, s);
         case 4:
-            if (R == 1) { if (GW == 8) QG_L(4, 1, 8, 8); QG_L(4, 1, 8, 4); }
-            if (R == 2 || FMT == FMT_Q4_K) { if (GW == 4) QG_L(4, 2, 8, 4); QG_L(4, 2, 8, 2); }
-            if constexpr (FMT != FMT_Q4_K) { if (GW == 2) QG_L(4, 4, 8, 2); QG_L(4, 4, 8, 1); }
-            return QG_ERR_UNSUPPORTED;
+            if (R <= 2) return dispatch_gw<FMT, 4, 8, 2>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 4, 8, 4>(dc, kp, GW, grid, smem, pdl, s);
         default:
-            if (R == 1 || FMT == FMT_Q4_K) { if (GW == 8) QG_L(8, 1, 8, 8); if (GW == 4) QG_L(8, 1, 8, 4); QG_L(8, 1, 8, 2); }
-            if constexpr (FMT != FMT_Q4_K) { if (GW == 4) QG_L(8, 2, 8, 4); QG_L(8, 2, 8, 2); }
-            return QG_ERR_UNSUPPORTED;
+            if (R <= 1) return dispatch_gw<FMT, 8, 8, 1>(dc, kp, GW, grid, smem, pdl, s);
+            if (R == 2) return dispatch_gw<FMT, 8, 8, 2>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 8, 8, 4>(dc, kp, GW, grid, smem, pdl, s);
     }
-#undef QG_L
 }
 
 }  // namespace fast
