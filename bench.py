@@ -363,10 +363,16 @@ def e2e_dual(r: Runner, steps: int, warmup: int):
 
 
 # -------------------------------------------------------------- traffic
+TRAFFIC_SOURCES = ("bit_quantized_gemv_dequant_gb300/csrc/gemv_fast.cuh",
+                   "bit_quantized_gemv_dequant_gb300/csrc/gemv.cu",
+                   "bit_quantized_gemv_dequant_gb300/csrc/gemv_fast_q4_0.cu",
+                   "bit_quantized_gemv_dequant_gb300/csrc/qg_internal.cuh")
+
+
 def source_hash():
+    """sha256 over the sources of the dual Q4_0 GEMV kernel and its planner."""
     h = hashlib.sha256()
-    for rel in ("bit_quantized_gemv_dequant_gb300/csrc/gemv.cu",
-                "bit_quantized_gemv_dequant_gb300/csrc/qg_internal.cuh"):
+    for rel in TRAFFIC_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
