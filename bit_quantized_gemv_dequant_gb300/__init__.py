@@ -29,7 +29,8 @@ QG_OPT_PDL = 1
 EXPORTS = ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_split",
            "dequant_q4_0", "dequant_q4_k", "dequant_affine", "qg_workspace_size",
            "qg_status_string", "qg_last_cuda_error", "qg_device_error",
-           "qg_selftest_wait_timeout", "qg_set_option", "qg_get_option")
+           "qg_selftest_wait_timeout", "qg_set_option", "qg_get_option",
+           "qgemv_q4_k_noalloc")
 
 _LIB = None
 _LOCK = threading.Lock()
@@ -72,6 +73,7 @@ def lib():
             "qg_selftest_wait_timeout": [I64, P],
             "qg_set_option": [I, I64],
             "qg_get_option": [I, C.POINTER(I64)],
+            "qgemv_q4_k_noalloc": [P, P, P, I64, I64, I64, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -172,6 +174,19 @@ def qgemv_q4_k(w, x, y=None, *, N=None, workspace=None, stream=None):
     _check(lib().qgemv_q4_k(_dev(w, "w", torch.uint8), _dev(x, "x", torch.float32),
                             _dev(y, "y", torch.float32), M, N, K, ws, wsb, _stream(stream)),
            "qgemv_q4_k")
+    return y
+
+
+def qgemv_q4_k_noalloc(w, x, y=None, *, N=None, stream=None):
+    """qgemv_q4_k without a caller workspace: split-K scratch lives in a fixed
+    4 MiB device array inside the library (see include/qgemv.h)."""
+    M, K = x.shape
+    N = N if N is not None else w.numel() // (K // 256 * 144)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(lib().qgemv_q4_k_noalloc(_dev(w, "w", torch.uint8), _dev(x, "x", torch.float32),
+                                    _dev(y, "y", torch.float32), M, N, K, _stream(stream)),
+           "qgemv_q4_k_noalloc")
     return y
 
 

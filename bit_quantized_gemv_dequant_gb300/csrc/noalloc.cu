@@ -1,0 +1,63 @@
+// qgemv_q4_k_noalloc: the Q4_K GEMV for callers that cannot allocate device
+// memory (for example code running inside a CUDA graph that was captured by
+// someone else, a plugin inside a host application that owns every device
+// allocation, or a runtime that forbids cudaMalloc after start-up). The
+// regular qgemv_q4_k needs a caller-provided workspace for its split-K
+// partial sums whenever x for all M rows does not fit in shared memory; this
+// variant uses a fixed-size scratch array that lives in the library's own
+// device memory instead.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "qg_internal.cuh"
+
+namespace qg {
+namespace {
+
+// Largest split-K scratch the entry point can use. Every GPU that loads the
+// library holds this array (4 MiB) until the process exits.
+constexpr size_t kNoAllocScratchBytes = 4u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDev = 64;
+std::once_flag g_once[kMaxDev];
+void* g_addr[kMaxDev];
+int g_rc[kMaxDev];
+
+// Device address of the scratch array on the current device. The host-side
+// name g_noalloc_scratch is only a stand-in for the symbol; the address a
+// kernel may use comes from cudaGetSymbolAddress, taken once per device with
+// that device current.
+int scratch_address(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDev) return QG_ERR_UNSUPPORTED;
+    std::call_once(g_once[dev], [dev] {
+        void* p = nullptr;
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        g_rc[dev] = (err == cudaSuccess) ? QG_OK : cuda_fail(err);
+        g_addr[dev] = p;
+    });
+    if (g_rc[dev] != QG_OK) return g_rc[dev];
+    *out = g_addr[dev];
+    return QG_OK;
+}
+
+}  // namespace
+}  // namespace qg
+
+extern "C" int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M, int64_t N,
+                                  int64_t K, qg_stream_t stream) {
+    size_t need = 0;
+    int rc = qg_workspace_size(QG_OP_Q4_K, M, N, K, 0, 0, &need);
+    if (rc != QG_OK) return rc;
+    if (need > qg::kNoAllocScratchBytes) return QG_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    rc = qg::scratch_address(&scratch);
+    if (rc != QG_OK) return rc;
+    // The split-K partial sums are fully written before they are read, so
+    // nothing in the scratch array needs clearing between calls.
+    return qgemv_q4_k(w, x, y, M, N, K, scratch, qg::kNoAllocScratchBytes, stream);
+}

@@ -115,6 +115,24 @@ QG_API int qgemv_dual_q4_0(const void* w_a, const void* w_b, const float* x, flo
 QG_API int qgemv_q4_k(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
                void* workspace, size_t workspace_bytes, qg_stream_t stream);
 
+/* qgemv_q4_k for callers that cannot call cudaMalloc (code inside someone
+ * else's CUDA graph capture, plugins whose host application owns every device
+ * allocation, runtimes that forbid allocation after start-up). No counterpart
+ * in the source pages: an addition of this library. Same arguments, result
+ * and accuracy as qgemv_q4_k, but the split-K scratch that qgemv_q4_k takes
+ * as a workspace comes from a 4 MiB array in the library's own device memory
+ * (held on every GPU that loads the library until the process exits).
+ * - Returns QG_ERR_WORKSPACE, before enqueuing anything, when the shape needs
+ *   more than 4 MiB of scratch (qg_workspace_size(QG_OP_Q4_K, ...) > 4 MiB).
+ * - Allocates nothing. The first call on a device looks up the array's device
+ *   address (cudaGetSymbolAddress); make that first call before any stream
+ *   capture.
+ * - All calls share the one array: calls that may overlap on the GPU (other
+ *   streams, other host threads) race on it. Its contents are fully rewritten
+ *   before they are read, so nothing needs clearing between calls. */
+QG_API int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M, int64_t N,
+                              int64_t K, qg_stream_t stream);
+
 /* Affine group-quantized matmul y = x . dequant(q, s, b)^T.
  * Page: qmm_affine.rs (mlx-native 0.21.1), dispatch_qmm_affine_t_f32 and
  * dispatch_qmm_affine_t_packed_simd4_b4 (packed 4-bit codes). The packed and
