@@ -456,6 +456,15 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(value: float) -> float:
+    """Maximum of a host-side float over all ranks (gloo process group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload_config(M):
     return {"workload": "fused dual Q4_0 projection: two Q4_0 weights N=K=4096 "
                         "(W ~ N(0,0.02^2)), shared x f32 [M,4096] ~ N(0,1)",
@@ -516,9 +525,7 @@ def main():
         sampler.stop()
     del graphs
     if dist:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms)
     us = 1000.0 * ms / args.steps
     value = world * r1.et_bytes * args.steps / (ms * 1e-3) / 1e9
     achieved = r1.et_bytes / (us * 1e3)
