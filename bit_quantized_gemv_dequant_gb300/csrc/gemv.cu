@@ -173,7 +173,7 @@ long long row_bytes(int fmt, long long K) {
 int r_options(int MT, int* out) {
     int n = 0;
     switch (MT) {
-        case 1: out[n++] = 2; out[n++] = 4; out[n++] = 8; break;
+        case 1: out[n++] = 2; out[n++] = 4; out[n++] = 8; out[n++] = 16; break;
         case 2: out[n++] = 2; out[n++] = 4; break;
         case 4: out[n++] = 2; out[n++] = 4; break;
         default: out[n++] = 1; out[n++] = 2; out[n++] = 4; break;
@@ -238,27 +238,33 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
         if (R > fast::max_rows(a.fmt, pl.MT)) continue;
         const int V = pl.MT * R;
         const int sums = g.sums ? pl.MT * pl.P * 32 * g.nh : 0;
-        const int xsum_bytes = ((sums + 2 * pl.W * V) * 4 + 127) & ~127;
         for (int co = 1; co >= 0; --co) {
             const int stage = ((R * pl.q_stride + 2 * R * pl.sb_stride + 16) + 127) & ~127;
             const int budget = co ? co_budget : dc.max_smem_optin;
-            const int avail = budget - pl.xs_bytes - xsum_bytes;
+            // Per stage: the copy, two mbarriers, an arrival counter and the
+            // group's partial sums (GW * V floats).
+            const int per_stage = stage + 16 + 4 + (pl.GW > 1 ? pl.GW * V * 4 : 0);
+            const int avail = budget - pl.xs_bytes - ((sums * 4 + 127) & ~127) - 128;
             if (avail <= 0) continue;
-            int S = std::min(kMaxStages, avail / (stage + 16));
+            int S = std::min(kMaxStages, avail / per_stage);
             if (S < 2) continue;
             if (S >= NG) S = NG * std::min(S / NG, 2);
+            const int xsum_bytes =
+                ((sums + S * (pl.GW > 1 ? pl.GW * V : 0) + S) * 4 + 127) & ~127;
             const long long spw = (a.N + R - 1) / R;
             const long long stages_total = spw * a.nw;
             const int grid = (int)std::min<long long>(stages_total, grid_cap);
             const double per_cta = (double)stages_total / grid;
             const int busy_groups = (int)std::min<double>(std::min(NG, S), std::ceil(per_cta));
             const int busy_warps = busy_groups * pl.GW;
-            // Lexicographic preference: most warps busy (>= 3/4 of them), then
-            // co-residency, then large copies, then row reuse of x, then warps.
-            const long long key = ((long long)(busy_warps * 4 >= pl.W * 3) << 40) |
-                                  ((long long)co << 36) | ((long long)(stage >= 14 * 1024) << 32) |
-                                  ((long long)R << 24) | ((long long)busy_warps << 16) |
-                                  (long long)S;
+            // Lexicographic preference (measured on GB300): most warps busy
+            // (>= 3/4 of them), then more rows per stage (x reuse, fewer
+            // per-stage costs), then two stages per group in flight, then
+            // co-residency with the next kernel, then large copies.
+            const long long key = ((long long)(busy_warps * 4 >= pl.W * 3) << 48) |
+                                  ((long long)R << 40) | ((long long)(S >= 2 * NG) << 36) |
+                                  ((long long)co << 32) | ((long long)(stage >= 14 * 1024) << 28) |
+                                  ((long long)busy_warps << 16) | (long long)S;
             if (key > best_key) {
                 best_key = key;
                 have = true;

@@ -305,6 +305,8 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
             mbar_init(smem_addr(&empty[i]), GW);
         }
         fence_mbar_init();
+        int* c0 = reinterpret_cast<int*>(smem + p.xs_bytes + p.xsum_bytes) - p.S;
+        for (int i = 0; i < p.S; ++i) c0[i] = 0;
     }
     __syncthreads();
 
@@ -388,17 +390,20 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
         const int span = p.P * PASS;
         const int quads = span >> 2;
         const bool vec = ((reinterpret_cast<uintptr_t>(p.x) & 15) == 0) && ((p.K & 3) == 0);
-        constexpr int QU = 16 / MT;  // quads per thread per round, for each of the MT rows
+        // Quads per thread per round, for each of the MT rows: at most 16
+        // loads in flight, and no more rounds than the slice needs.
+        constexpr int QU = 16 / MT;
+        const int per_thread = (quads + kThreadsC - 1) / kThreadsC;
 #pragma unroll 1
-        for (int q0 = threadIdx.x; q0 < quads; q0 += QU * kThreadsC) {
+        for (int u0 = 0; u0 < per_thread; u0 += QU) {
             float4 v[QU][MT];
 #pragma unroll
             for (int u = 0; u < QU; ++u) {
-                const int e = (q0 + u * kThreadsC) << 2;
+                const int e = (threadIdx.x + (u0 + u) * kThreadsC) << 2;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     v[u][m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (m < p.M && e < p.klen) {
+                    if (u0 + u < per_thread && m < p.M && e < p.klen) {
                         const float* src = p.x + (long long)m * p.K + k0 + e;
                         if (vec) {
                             v[u][m] = *reinterpret_cast<const float4*>(src);
@@ -410,10 +415,12 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                         }
                     }
                 }
+                if (u0 + u + 1 >= per_thread) break;
             }
 #pragma unroll
             for (int u = 0; u < QU; ++u) {
-                const int e = (q0 + u * kThreadsC) << 2;
+                if (u0 + u >= per_thread) break;
+                const int e = (threadIdx.x + (u0 + u) * kThreadsC) << 2;
                 if (e >= span) break;
                 const int pp = e >> LOG_PASS, within = e & (PASS - 1);
                 const int ln = within >> LOG_UE, j = within & (UE - 1);
@@ -458,10 +465,11 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
     const uint32_t mg = p.magic;
     float2 cst[4];
     if (FMT != FMT_AFF_U8) decode_consts<FMT>(cst);
-    // Cross-warp partial sums of a group: [2 (stage parity)][NG][GW][V], kept
-    // in the last red_floats() floats of the x-sum region.
+    // Cross-warp partial sums of a stage, [S][GW][V], and per-stage arrival
+    // counters, [S], kept at the end of the x-sum region (see the planner).
     constexpr int V = MT * R;
-    float* red = xsum + (p.xsum_bytes >> 2) - 2 * W * V;
+    int* cnt = reinterpret_cast<int*>(xsum + (p.xsum_bytes >> 2)) - p.S;
+    float* red = reinterpret_cast<float*>(cnt) - p.S * GW * V;
 
     // Stage st is consumed only by warp group st % NG (see the file comment):
     // with S a multiple of NG group g takes stages g, g+NG, ...; with S < NG,
@@ -487,9 +495,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
         const uint8_t* stg = stages + (size_t)st * p.stage_bytes;
         // Rows past the end of a matrix (ragged last stage) are computed from
         // stale stage bytes and never written.
-        const uint8_t* rowp[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) rowp[r] = stg + r * p.q_stride;
 
         float acc[MT][R];
 #pragma unroll
@@ -528,8 +533,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
 #pragma unroll
                 for (int b = 0; b < RB; ++b) {
                     const int r = rb0 + b;
+                    const uint8_t* rowr = stg + r * p.q_stride;
                     if (FMT == FMT_Q4_0) {
-                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowp[r] + (ub & ~3));
+                        const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowr + (ub & ~3));
 #pragma unroll
                         for (int q = 0; q < 5; ++q) win[b][q] = wp[q];
                         const uint32_t dbits =
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                         us[b].a0 = __half2float(__ushort_as_half((unsigned short)dbits));
                     } else if (FMT == FMT_Q4_K) {
                         const int c = uc & 3;
-                        const uint4 h = *reinterpret_cast<const uint4*>(rowp[r] + (uc >> 2) * 144);
+                        const uint4 h = *reinterpret_cast<const uint4*>(rowr + (uc >> 2) * 144);
                         int sc0, mn0, sc1, mn1;
                         q4k_pair(h.y, h.z, h.w, 2 * c, sc0, mn0);
                         q4k_pair(h.y, h.z, h.w, 2 * c + 1, sc1, mn1);
@@ -576,17 +582,17 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                     }
 #pragma unroll
                     for (int b = 0; b < RB; ++b) {
-                        const int r = rb0 + b;
+                        const uint8_t* rowr = stg + (rb0 + b) * p.q_stride;
                         float2 f[4];
                         if (FMT == FMT_Q4_0) {
                             decode_nibbles<FMT>(__funnelshift_rc(win[b][w], win[b][w + 1], qsh), mg,
                                                 cst, f);
                         } else if (FMT == FMT_Q4_K || FMT == FMT_AFF_PACKED) {
                             const uint32_t v =
-                                *reinterpret_cast<const uint32_t*>(rowp[r] + qo + 4 * w);
+                                *reinterpret_cast<const uint32_t*>(rowr + qo + 4 * w);
                             decode_nibbles<FMT>(v, mg, cst, f);
                         } else {
-                            const uint2 v = *reinterpret_cast<const uint2*>(rowp[r] + qo + 8 * w);
+                            const uint2 v = *reinterpret_cast<const uint2*>(rowr + qo + 8 * w);
                             decode_bytes(v.x, v.y, mg, f);
                         }
 #pragma unroll
@@ -625,9 +631,6 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
-
         float vals[V];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
@@ -638,17 +641,28 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
         const bool holder = (lane % kSpan) == 0;
         const int v = lane / kSpan;
         float total = vals[0];
+        bool writer = true;
         if (GW > 1) {
-            float* rb = red + (((use & 1) * NG + grp) * GW) * V;
-            if (holder) rb[gw * V + v] = total;
-            named_bar_sync(2 + grp, GW * 32);
-            if (gw == 0 && holder) {
-                total = rb[v];
+            // The last warp of the group to finish this stage adds the GW
+            // partial sums in warp order; the others move on without waiting.
+            float* rs = red + (size_t)st * GW * V;
+            if (holder) rs[gw * V + v] = total;
+            __threadfence_block();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = (atomicAdd(&cnt[st], 1) == GW - 1);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            writer = last != 0;
+            if (writer) {
+                __threadfence_block();
+                total = rs[v];
 #pragma unroll
-                for (int g2 = 1; g2 < GW; ++g2) total += rb[g2 * V + v];
+                for (int g2 = 1; g2 < GW; ++g2) total += rs[g2 * V + v];
+                __syncwarp();
+                if (lane == 0) cnt[st] = 0;
             }
         }
-        if (gw == 0 && holder) {
+        if (writer && holder) {
             const int m = v / R, r = v % R;
             if (m < p.M && r < rows) {
                 const long long o = (long long)m * p.N + row0 + r;
@@ -658,6 +672,10 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                     p.partial[((long long)(ks * p.nw + wi) * p.M) * p.N + o] = total;
             }
         }
+        // The stage (and its partial-sum slot) is released only after this
+        // warp is done with both.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
         st += stride;
         if (st >= p.S) {
             st -= p.S;
@@ -702,9 +720,9 @@ namespace fast {
 // Largest rows-per-stage per (format, M bucket) that compiles without
 // register spills (16 consumer warps cap a thread at 96 registers, 8 at 168).
 __host__ __device__ constexpr int max_rows(int fmt, int MT) {
-    return fmt == FMT_Q4_0   ? (MT == 1 ? 8 : MT == 8 ? 2 : 4)
+    return fmt == FMT_Q4_0   ? (MT == 1 ? 16 : MT == 8 ? 2 : 4)
            : fmt == FMT_Q4_K ? (MT == 1 ? 4 : MT == 8 ? 1 : 2)
-                             : (MT == 1 ? 8 : 2);
+                             : (MT == 1 ? 16 : 2);
 }
 
 // (MT, R, GW) -> kernel instantiation: R rows per stage, shared by a group of
@@ -730,7 +748,8 @@ int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int grid
         case 1:
             if (R <= 2) return dispatch_gw<FMT, 1, 16, 2>(dc, kp, GW, grid, smem, pdl, s);
             if (R == 4) return dispatch_gw<FMT, 1, 16, 4>(dc, kp, GW, grid, smem, pdl, s);
-            return dispatch_gw<FMT, 1, 16, 8>(dc, kp, GW, grid, smem, pdl, s);
+            if (R == 8) return dispatch_gw<FMT, 1, 16, 8>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 1, 16, 16>(dc, kp, GW, grid, smem, pdl, s);
         case 2:
             if (R <= 2) return dispatch_gw<FMT, 2, 16, 2>(dc, kp, GW, grid, smem, pdl, s);
             return dispatch_gw<FMT, 2, 16, 4>(dc, kp, GW, grid, smem, pdl, s);
