@@ -1,0 +1,627 @@
+// Affine-quantized matmul for many activation rows (prefill) on the fifth-
+// generation tensor cores.
+//
+// Page: qmm_affine.rs (mlx-native 0.21.1), dispatch_qmm_affine_t_f32 and the
+// packed 4-bit variant: y[m,n] = sum_k x[m,k] * w[n,k], w[n,k] = s[n,g] *
+// q[n,k] + b[n,g], g = k / gs. Regrouping the sum per quantization group,
+//
+//     y[m,n] = sum_g ( s[n,g] * P_g[n,m] + b[n,g] * X_g[m] ),
+//     P_g[n,m] = sum_{k in g} q[n,k] * x[m,k],   X_g[m] = sum_{k in g} x[m,k],
+//
+// the inner sums P_g are a plain integer-weight contraction, which runs here
+// as tcgen05 MMAs: the codes q (integers 0..255) are exact in fp16, and x is
+// rounded to fp16 once. The same page's bf16 table-plus-sums kernels (the
+// K9/K10 section) split the sum the same way; this kernel keeps the integer
+// codes exact and applies scale and bias in an f32 epilogue.
+//
+// Two launches per call:
+//   prep: for each activation row m, a power-of-two scale 2^e_m (so that the
+//         largest |x| lands in [2^14, 2^15) and fp16 neither overflows nor
+//         goes subnormal early), xh = fp16_rn(x * 2^e_m), and X_g[m] summed in
+//         f32 from the ROUNDED values. Using the rounded values in both terms
+//         makes the factored sum equal sum_k w * xh up to f32 rounding, so the
+//         error is at most 2^-11 * sum_k |w * x| plus f32 rounding.
+//   main: one CTA per (128 weight rows) x (128 activation rows) tile.
+//         warp 12      TMA producer: per 64-wide k chunk, the code tile
+//                      (128 rows, u8 or packed) and the xh tile (128 rows,
+//                      fp16, 128-byte swizzle) into a ring of stages.
+//         warps 0-3    converters: codes -> fp16 (exact) in registers, stored
+//                      into tensor memory as the A operand (tcgen05.st); the
+//                      converted weights never pass through shared memory.
+//         warp 13      MMA issuer: kind::f16, M=128 (weight rows), N=128
+//                      (activation rows), K=16 per instruction, f32
+//                      accumulators P_g in tensor memory, two buffers.
+//         warps 4-11   epilogue: acc += s * P_g + b * X_g per group, in f32
+//                      registers; at the end y = acc * 2^-e_m.
+// Every wait is bounded; a wait that runs out records an error bit and the
+// CTA winds down (drains its copies and MMAs, frees tensor memory) instead of
+// hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "qg_internal.cuh"
+
+namespace qg {
+namespace prefill {
+
+constexpr int kTileN = 128;    // weight rows per CTA (MMA M)
+constexpr int kTileT = 128;    // activation rows per CTA (MMA N)
+constexpr int kChunk = 64;     // k per stage (one 128-byte fp16 row)
+constexpr int kStages = 8;
+constexpr int kABufs = 4;      // A operand buffers in tensor memory (32 columns each)
+constexpr int kPCols = kTileT; // columns per P buffer
+constexpr int kACol0 = 2 * kPCols;
+constexpr int kTmemCols = 512;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
+constexpr int kXhBytes = kTileT * kChunk * 2;  // 16 KB per stage
+constexpr int kPrepThreads = 256;
+
+struct Params {
+    const float* scales;   // [N, G]
+    const float* biases;   // [N, G]
+    float* y;              // [M, N]
+    const float* xsum;     // [G, Mp] group sums of the rounded activations
+    const float* inv;      // [Mp] 2^-e_m
+    int M, N, K, G, Mp;
+    int log2_spg;          // log2(gs / 16): MMA k-steps per group
+    unsigned* err;
+};
+
+template <bool PACKED>
+struct Geo {
+    static constexpr int kCodeRowBytes = PACKED ? kChunk / 2 : kChunk;    // per stage
+    static constexpr int kCodeBytes = kTileN * kCodeRowBytes;
+    static constexpr int kStageBytes = kXhBytes + kCodeBytes;             // multiple of 1024
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOff + 512;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; fp16 inputs, f32 accumulate.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's lane, waited on in the same
+// statement so no use of the registers can be scheduled before the data.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in 128-byte swizzle atoms
+// (8 rows x 128 bytes, atoms 1024 bytes apart), start address in 16-byte units.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, fp16 A and B, both
+// K-major, N = kTileT, M = kTileN.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kTileT >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
+
+// Four u8 codes (little-endian bytes of v) -> two fp16x2 words holding the
+// exact values: 0x64 above each byte is 1024 + q, minus 1024 leaves q.
+__device__ __forceinline__ void codes4_to_h2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+    const uint32_t a = __byte_perm(v, 0x6464u, 0x4140u);
+    const uint32_t b = __byte_perm(v, 0x6464u, 0x4342u);
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64006400u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64006400u));
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------- prep kernel
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restrict__ x,
+                                                            __half* __restrict__ xh,
+                                                            float* __restrict__ xsum,
+                                                            float* __restrict__ inv, int M, int K,
+                                                            int gs, int G, int Mp) {
+    __shared__ float red[kPrepThreads / 32];
+    __shared__ float amax_s;
+    const int m = blockIdx.x;
+    const int t = threadIdx.x;
+    const int lane = t & 31, warp = t >> 5;
+    if (m >= M) {  // padding rows: zero group sums so the epilogue reads defined values
+        for (int g = t; g < G; g += kPrepThreads) xsum[(size_t)g * Mp + m] = 0.f;
+        if (t == 0) inv[m] = 1.f;
+        return;
+    }
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)m * K);
+    const int quads = K >> 2;
+    float amax = 0.f;
+    for (int c = t; c < quads; c += kPrepThreads) {
+        const float4 v = __ldg(xr + c);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    if (t == 0) {
+        float a = red[0];
+        for (int w = 1; w < kPrepThreads / 32; ++w) a = fmaxf(a, red[w]);
+        amax_s = a;
+    }
+    __syncthreads();
+    amax = amax_s;
+    int e = 0;
+    if (amax > 0.f && amax <= 3.402823466e38f) {
+        int ex;
+        frexpf(amax, &ex);         // amax = f * 2^ex, f in [0.5, 1)
+        e = min(126, max(-126, 15 - ex));
+    }
+    const float scale = ldexpf(1.f, e);
+    if (t == 0) inv[m] = ldexpf(1.f, -e);
+    __syncthreads();  // red[] is reused below
+
+    // Threads t .. t + gs/4 - 1 of one pass hold one group (1024 = 4 * 256 is a
+    // multiple of every gs <= 1024, so a group never straddles two passes).
+    const int width = min(gs >> 2, 32);
+    const int groups_per_pass = (4 * kPrepThreads) / gs;  // 0 when gs > 1024 (not allowed)
+    __half2* xo = reinterpret_cast<__half2*>(xh + (size_t)m * K);
+    for (int base = 0; base < quads; base += kPrepThreads) {
+        const int c = base + t;
+        float f = 0.f;
+        if (c < quads) {
+            const float4 v = __ldg(xr + c);
+            const __half2 h0 = __floats2half2_rn(v.x * scale, v.y * scale);
+            const __half2 h1 = __floats2half2_rn(v.z * scale, v.w * scale);
+            xo[2 * c] = h0;
+            xo[2 * c + 1] = h1;
+            const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+            f = (f0.x + f0.y) + (f1.x + f1.y);
+        }
+        for (int o = width >> 1; o; o >>= 1) f += __shfl_xor_sync(0xFFFFFFFFu, f, o);
+        if ((gs >> 2) <= 32) {
+            if ((lane & (width - 1)) == 0 && c < quads) {
+                const int g = (c << 2) >> (__ffs(gs) - 1);
+                xsum[(size_t)g * Mp + m] = f;
+            }
+        } else {
+            if (lane == 0) red[warp] = f;
+            __syncthreads();
+            const int wpg = gs >> 7;  // warps per group
+            if (t < groups_per_pass) {
+                float s = 0.f;
+                for (int w = 0; w < wpg; ++w) s += red[t * wpg + w];
+                const int g = base / (gs >> 2) + t;
+                if (g < G) xsum[(size_t)g * Mp + m] = s;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ------------------------------------------------------------- main kernel
+template <bool PACKED>
+__global__ void __launch_bounds__(kThreads, 1)
+    mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_x,
+               const Params p) {
+    using Gm = Geo<PACKED>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t bars = base + Gm::kBarOff;
+    auto full = [&](int i) { return bars + 8u * i; };
+    auto empty = [&](int i) { return bars + 8u * (kStages + i); };
+    auto a_full = [&](int i) { return bars + 8u * (2 * kStages + i); };
+    auto a_empty = [&](int i) { return bars + 8u * (2 * kStages + kABufs + i); };
+    auto p_full = [&](int i) { return bars + 8u * (2 * kStages + 2 * kABufs + i); };
+    auto p_empty = [&](int i) { return bars + 8u * (2 * kStages + 2 * kABufs + 2 + i); };
+    const uint32_t done_bar = bars + 8u * (2 * kStages + 2 * kABufs + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + 8 * (2 * kStages + 2 * kABufs + 5));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTileT;
+    const int n0 = blockIdx.y * kTileN;
+    const int nstages = (p.K + kChunk - 1) / kChunk;
+    const int nks = p.K >> 4;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full(i), 1);
+            mbar_init(empty(i), 1);
+        }
+        for (int i = 0; i < kABufs; ++i) {
+            mbar_init(a_full(i), 128);
+            mbar_init(a_empty(i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(p_full(i), 1);
+            mbar_init(p_empty(i), 256);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&map_q);
+            prefetch_tmap(&map_x);
+            int issued = 0;
+            for (int i = 0; i < nstages; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages && !mbar_wait(empty(st), ((i / kStages) & 1) ^ 1)) {
+                    report_error(p.err, DEVERR_TC_WAIT);
+                    break;
+                }
+                const uint32_t sb = base + st * Gm::kStageBytes;
+                mbar_arrive_expect_tx(full(st), Gm::kStageBytes);
+                tma_load_2d(sb, &map_x, i * kChunk, m0, full(st));
+                tma_load_2d(sb + kXhBytes, &map_q, i * Gm::kCodeRowBytes, n0, full(st));
+                issued = i + 1;
+            }
+            // Copies must land before the CTA can exit, whatever happened above.
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                if (!mbar_wait(full(i % kStages), (i / kStages) & 1))
+                    report_error(p.err, DEVERR_WAIT_DRAIN);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const int spg_mask = (1 << p.log2_spg) - 1;
+            for (int ks = 0; ks < nks; ++ks) {
+                const int i = ks >> 2, kk = ks & 3;
+                const int j = ks >> p.log2_spg;
+                const bool first = (ks & spg_mask) == 0;
+                const bool last = (ks & spg_mask) == spg_mask;
+                if (kk == 0) {
+                    if (!mbar_wait(full(i % kStages), (i / kStages) & 1) ||
+                        !mbar_wait(a_full(i % kABufs), (i / kABufs) & 1)) {
+                        report_error(p.err, DEVERR_TC_WAIT);
+                        break;
+                    }
+                }
+                if (first && j >= 2 && !mbar_wait(p_empty(j & 1), ((j >> 1) & 1) ^ 1)) {
+                    report_error(p.err, DEVERR_TC_WAIT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sb = base + (i % kStages) * Gm::kStageBytes;
+                tc_mma_ts(tmem + (j & 1) * kPCols, tmem + kACol0 + (i % kABufs) * 32 + kk * 8,
+                          sw128_desc(sb + kk * 32), kIdesc, first ? 0u : 1u);
+                if (last) tc_commit(p_full(j & 1));
+                if (kk == 3 || ks == nks - 1) {
+                    tc_commit(empty(i % kStages));
+                    tc_commit(a_empty(i % kABufs));
+                }
+            }
+            tc_commit(done_bar);
+            if (!mbar_wait(done_bar, 0)) report_error(p.err, DEVERR_WAIT_DRAIN);
+        }
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- converters
+        const int row = threadIdx.x;  // 0..127: lane 32*warp + lane of tensor memory
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        for (int i = 0; i < nstages; ++i) {
+            const int st = i % kStages, ab = i % kABufs;
+            if (!warp_wait(full(st), (i / kStages) & 1) ||
+                (i >= kABufs && !warp_wait(a_empty(ab), ((i / kABufs) & 1) ^ 1))) {
+                if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
+                break;
+            }
+            tc_fence_after();
+            const uint8_t* cb = smem + st * Gm::kStageBytes + kXhBytes;
+            const uint32_t acol = tmem + lane_base + kACol0 + ab * 32;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t h[16];
+                if (!PACKED) {
+                    // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * hf + cc;
+                        const uint4 v = *reinterpret_cast<const uint4*>(
+                            cb + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                        codes4_to_h2(v.x, h[8 * cc + 0], h[8 * cc + 1]);
+                        codes4_to_h2(v.y, h[8 * cc + 2], h[8 * cc + 3]);
+                        codes4_to_h2(v.z, h[8 * cc + 4], h[8 * cc + 5]);
+                        codes4_to_h2(v.w, h[8 * cc + 6], h[8 * cc + 7]);
+                    }
+                } else {
+                    // 32-byte swizzle: chunk c of row r sits at chunk c ^ ((r >> 2) & 1).
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        cb + row * 32 + ((hf ^ ((row >> 2) & 1)) << 4));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // low nibble of each byte = even k, high nibble = odd k
+                        const uint32_t lo = w4[e] & 0x0F0F0F0Fu;
+                        const uint32_t hi = (w4[e] >> 4) & 0x0F0F0F0Fu;
+                        codes4_to_h2(__byte_perm(lo, hi, 0x5140u), h[4 * e + 0], h[4 * e + 1]);
+                        codes4_to_h2(__byte_perm(lo, hi, 0x7362u), h[4 * e + 2], h[4 * e + 3]);
+                    }
+                }
+                tmem_st16(acol + hf * 16, h);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(a_full(ab));
+        }
+    } else if (warp < 12) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // tensor-memory lane quarter
+        const int half = (warp - 4) >> 2;       // which 64 activation rows
+        const int n = n0 + q * 32 + lane;
+        const bool nvalid = n < p.N;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int t0 = m0 + half * 64;
+        float2 acc[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.f, 0.f);
+        bool ok = true;
+        const float* srow = p.scales + (size_t)(nvalid ? n : 0) * p.G;
+        const float* brow = p.biases + (size_t)(nvalid ? n : 0) * p.G;
+        for (int j = 0; j < p.G; ++j) {
+            const int pb = j & 1;
+            const float s = nvalid ? __ldg(srow + j) : 0.f;
+            const float b = nvalid ? __ldg(brow + j) : 0.f;
+            const float2 s2 = make_float2(s, s), b2 = make_float2(b, b);
+            const float4* xs = reinterpret_cast<const float4*>(p.xsum + (size_t)j * p.Mp + t0);
+            if (!warp_wait(p_full(pb), (j >> 1) & 1)) {
+                if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int hf = 0; hf < 4; ++hf) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lane_base + pb * kPCols + half * 64 + hf * 16, r);
+                if (hf == 3) {
+                    tc_fence_before();
+                    mbar_arrive(p_empty(pb));
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const float4 xv = __ldg(xs + hf * 4 + c4);
+                    const int c = hf * 8 + c4 * 2;
+                    float2 t = __ffma2_rn(b2, make_float2(xv.x, xv.y), acc[c]);
+                    acc[c] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4]),
+                                                        __uint_as_float(r[4 * c4 + 1])), t);
+                    t = __ffma2_rn(b2, make_float2(xv.z, xv.w), acc[c + 1]);
+                    acc[c + 1] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4 + 2]),
+                                                            __uint_as_float(r[4 * c4 + 3])), t);
+                }
+            }
+        }
+        if (ok) {
+            // Lane l holds 2^-e of activation rows t0 + 2l and t0 + 2l + 1.
+            const float2 iv = __ldg(reinterpret_cast<const float2*>(p.inv + t0) + lane);
+            float* yp = p.y + (size_t)t0 * p.N + (nvalid ? n : 0);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float2 sc = make_float2(__shfl_sync(0xFFFFFFFFu, iv.x, c),
+                                              __shfl_sync(0xFFFFFFFFu, iv.y, c));
+                const int m = t0 + 2 * c;
+                if (nvalid && m < p.M) *yp = acc[c].x * sc.x;
+                yp += p.N;
+                if (nvalid && m + 1 < p.M) *yp = acc[c].y * sc.y;
+                yp += p.N;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_rc = cudaSuccess;
+
+int encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        g_encode_rc = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                       cudaEnableDefault, &q);
+        if (g_encode_rc == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (g_encode_rc != cudaSuccess) return cuda_fail(g_encode_rc);
+    if (!g_encode) return QG_ERR_UNSUPPORTED;
+    *out = g_encode;
+    return QG_OK;
+}
+
+struct Layout {
+    size_t xh, xsum, inv, total;
+    int Mp, G;
+};
+
+Layout layout(const GemvArgs& a) {
+    Layout L{};
+    L.Mp = (int)((a.M + kTileT - 1) / kTileT * kTileT);
+    L.G = (int)(a.K / a.gs);
+    auto up = [](size_t v) { return (v + 1023) & ~(size_t)1023; };
+    L.xh = 0;
+    L.xsum = up((size_t)a.M * a.K * 2);
+    L.inv = L.xsum + up((size_t)L.G * L.Mp * 4);
+    L.total = L.inv + up((size_t)L.Mp * 4);
+    return L;
+}
+
+template <bool PACKED>
+int launch_main(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx, const Params& kp,
+                dim3 grid, cudaStream_t s) {
+    constexpr int smem = Geo<PACKED>::kSmemBytes;
+    static int configured[64] = {0};
+    auto kern = mma_kernel<PACKED>;
+    if (dc.device >= 0 && dc.device < 64 && !configured[dc.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured[dc.device] = 1;
+    }
+    kern<<<grid, kThreads, smem, s>>>(mq, mx, kp);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
+}  // namespace prefill
+
+bool prefill_eligible(const DevCtx& dc, const GemvArgs& a) {
+    const bool packed = a.fmt == FMT_AFF_PACKED;
+    if (a.fmt != FMT_AFF_U8 && !packed) return false;
+    if (a.M < launch_option(QG_OPT_PREFILL_MIN_M)) return false;
+    if (a.gs < 16) return false;
+    if (a.K % (packed ? 32 : 16)) return false;
+    if (a.K > (1ll << 30) || a.M > (1ll << 30)) return false;
+    if (a.N > 65535ll * prefill::kTileN) return false;
+    if ((reinterpret_cast<uintptr_t>(a.w[0]) & 15) || (reinterpret_cast<uintptr_t>(a.x) & 15))
+        return false;
+    if (dc.max_smem_optin < prefill::Geo<false>::kSmemBytes) return false;
+    return true;
+}
+
+size_t prefill_workspace_bytes(const GemvArgs& a) { return prefill::layout(a).total; }
+
+int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
+    using namespace prefill;
+    const Layout L = layout(a);
+    if (!ws || ws_bytes < L.total) return QG_ERR_WORKSPACE;
+    const bool packed = a.fmt == FMT_AFF_PACKED;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    int rc = encoder(&encode);
+    if (rc) return rc;
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    __half* xh = reinterpret_cast<__half*>(w8 + L.xh);
+    float* xsum = reinterpret_cast<float*>(w8 + L.xsum);
+    float* inv = reinterpret_cast<float*>(w8 + L.inv);
+
+    CUtensorMap mx, mq;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+        const cuuint32_t box[2] = {kChunk, kTileT};
+        const cuuint32_t es[2] = {1, 1};
+        if (encode(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QG_ERR_UNSUPPORTED;
+    }
+    {
+        const cuuint64_t kb = packed ? a.K / 2 : a.K;
+        const cuuint64_t dims[2] = {kb, (cuuint64_t)a.N};
+        const cuuint64_t strides[1] = {kb};
+        const cuuint32_t box[2] = {(cuuint32_t)(packed ? kChunk / 2 : kChunk), kTileN};
+        const cuuint32_t es[2] = {1, 1};
+        if (encode(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.w[0]), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   packed ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QG_ERR_UNSUPPORTED;
+    }
+
+    prep_kernel<<<L.Mp, kPrepThreads, 0, s>>>(a.x, xh, xsum, inv, (int)a.M, (int)a.K, a.gs, L.G, L.Mp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    Params kp{};
+    kp.scales = a.scales;
+    kp.biases = a.biases;
+    kp.y = a.y[0];
+    kp.xsum = xsum;
+    kp.inv = inv;
+    kp.M = (int)a.M;
+    kp.N = (int)a.N;
+    kp.K = (int)a.K;
+    kp.G = L.G;
+    kp.Mp = L.Mp;
+    int l = 0;
+    while ((16 << l) < a.gs) ++l;
+    kp.log2_spg = l;
+    kp.err = dc.err;
+    const dim3 grid(L.Mp / kTileT, (unsigned)((a.N + kTileN - 1) / kTileN));
+    return packed ? launch_main<true>(dc, mq, mx, kp, grid, s)
+                  : launch_main<false>(dc, mq, mx, kp, grid, s);
+}
+
+}  // namespace qg

@@ -23,6 +23,7 @@ std::once_flag g_once[kMaxDevices];
 int g_ctx_rc[kMaxDevices];
 thread_local int t_last_cuda_error = 0;
 std::atomic<long long> g_opt_pdl{0};
+std::atomic<long long> g_opt_prefill_min_m{16};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -127,6 +128,10 @@ int run_gemv(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
     const DevCtx* dc = nullptr;
     rc = current_ctx(&dc);
     if (rc) return rc;
+    if (prefill_eligible(*dc, a)) {
+        if (prefill_workspace_bytes(a) > (ws ? ws_bytes : 0)) return QG_ERR_WORKSPACE;
+        return prefill_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    }
     if (gemv_workspace_bytes(*dc, a) > (ws ? ws_bytes : 0)) return QG_ERR_WORKSPACE;
     return gemv_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -134,7 +139,11 @@ int run_gemv(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
 }  // namespace
 
 long long launch_option(int option) {
-    return option == QG_OPT_PDL ? g_opt_pdl.load(std::memory_order_relaxed) : 0;
+    switch (option) {
+        case QG_OPT_PDL: return g_opt_pdl.load(std::memory_order_relaxed);
+        case QG_OPT_PREFILL_MIN_M: return g_opt_prefill_min_m.load(std::memory_order_relaxed);
+        default: return 0;
+    }
 }
 
 int cuda_fail(cudaError_t e) {
@@ -290,11 +299,12 @@ int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_size, i
     // caller's buffers allow the fastest path (an upper bound otherwise).
     static const uint8_t probe[16] __attribute__((aligned(16))) = {0};
     a.w[0] = a.w[1] = probe;
-    a.scales = a.biases = reinterpret_cast<const float*>(probe);
+    a.scales = a.biases = a.x = reinterpret_cast<const float*>(probe);
     const DevCtx* dc = nullptr;
     rc = current_ctx(&dc);
     if (rc) return rc;
     *bytes = gemv_workspace_bytes(*dc, a);
+    if (prefill_eligible(*dc, a)) *bytes = std::max(*bytes, prefill_workspace_bytes(a));
     return QG_OK;
 }
 
@@ -304,6 +314,10 @@ int qg_set_option(int option, int64_t value) {
             if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
             g_opt_pdl.store(value, std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_PREFILL_MIN_M:
+            if (value < 1) return QG_ERR_INVALID_ARG;
+            g_opt_prefill_min_m.store(value, std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }
@@ -312,6 +326,9 @@ int qg_get_option(int option, int64_t* value) {
     if (!value) return QG_ERR_INVALID_ARG;
     switch (option) {
         case QG_OPT_PDL: *value = g_opt_pdl.load(std::memory_order_relaxed); return QG_OK;
+        case QG_OPT_PREFILL_MIN_M:
+            *value = g_opt_prefill_min_m.load(std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }

@@ -17,6 +17,7 @@ enum : unsigned {
     DEVERR_WAIT_EMPTY = 2u,     // producer gave up waiting for a stage to drain
     DEVERR_WAIT_DRAIN = 4u,     // copies still in flight after an error
     DEVERR_SELFTEST = 8u,       // the self-test wait ran out (expected)
+    DEVERR_TC_WAIT = 16u,       // a tensor-core pipeline role gave up waiting
 };
 
 // Bounded waits give up after this many nanoseconds.
@@ -133,6 +134,13 @@ struct GemvArgs {
 
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a);
 int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+
+// Affine prefill on the tensor cores (prefill.cu). Eligibility depends on the
+// shape, the group size, the code and activation pointers' alignment and the
+// QG_OPT_PREFILL_MIN_M option.
+bool prefill_eligible(const DevCtx& dc, const GemvArgs& a);
+size_t prefill_workspace_bytes(const GemvArgs& a);
+int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 
 // Copies and dequantization (elementwise.cu).
 int qkv_split_launch(const DevCtx& dc, const float* qkv, float* q, float* k, float* v,

@@ -136,8 +136,22 @@ QG_API int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M
 /* Affine group-quantized matmul y = x . dequant(q, s, b)^T.
  * Page: qmm_affine.rs (mlx-native 0.21.1), dispatch_qmm_affine_t_f32 and
  * dispatch_qmm_affine_t_packed_simd4_b4 (packed 4-bit codes). The packed and
- * one-code-per-byte storages give bitwise-identical y. M up to 8 runs on CUDA
- * cores; larger M is a prefill contraction. */
+ * one-code-per-byte storages give bitwise-identical y.
+ *
+ * Two paths, chosen per call:
+ * - CUDA cores, f32 throughout (|y - exact| <= 1e-5 * sum_k |x w| + 1e-6):
+ *   M below the QG_OPT_PREFILL_MIN_M option (default 16), or any of the
+ *   tensor-core conditions below unmet.
+ * - Tensor cores (prefill), when M >= QG_OPT_PREFILL_MIN_M, group_size >= 16,
+ *   K % 16 == 0 (K % 32 == 0 when packed), q and x 16-byte aligned, M, N, K
+ *   <= 2^30 and N <= 8,388,480. Each x row is scaled by a power of two and
+ *   rounded to fp16 once; the codes enter the MMA as exact fp16 integers and
+ *   per-group f32 partial sums get scale and bias in an f32 epilogue (the
+ *   regrouping the page's bf16 table-plus-sums kernels use). Error:
+ *   |y - exact| <= 2^-11 * sum_k |x w| plus f32 rounding; callers should
+ *   budget 2e-3 * sum_k |x w|. Needs a workspace of qg_workspace_size bytes
+ *   (the fp16 copy of x plus per-group sums).
+ * Non-finite x propagates to the affected y rows on both paths. */
 QG_API int qmm_affine(const float* x, const void* q, const float* scales, const float* biases, float* y,
                int64_t M, int64_t N, int64_t K, int group_size, int packed, void* workspace,
                size_t workspace_bytes, qg_stream_t stream);
@@ -174,7 +188,10 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * written by the kernel immediately preceding it on the stream (static model
  * weights satisfy this). Back-to-back decode projections overlap one call's
  * ramp-up with the previous call's tail this way. */
-enum { QG_OPT_PDL = 1 };
+/*
+ * QG_OPT_PREFILL_MIN_M (default 16, >= 1): smallest M for which qmm_affine
+ * takes the tensor-core prefill path (when its other conditions hold). */
+enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2 };
 QG_API int qg_set_option(int option, int64_t value);
 QG_API int qg_get_option(int option, int64_t* value);
 
