@@ -53,8 +53,11 @@ constexpr int kTileT = 128;    // activation rows per CTA (MMA N)
 constexpr int kChunk = 64;     // k per stage (one 128-byte fp16 row)
 constexpr int kStages = 8;
 constexpr int kABufs = 4;      // A operand buffers in tensor memory (32 columns each)
+constexpr int kPBufs = 3;      // P_g accumulators in tensor memory
 constexpr int kPCols = kTileT; // columns per P buffer
-constexpr int kACol0 = 2 * kPCols;
+constexpr int kACol0 = kPBufs * kPCols;  // A buffers follow: 384 + 4 * 32 = 512 columns
+constexpr int kXSlots = 8;     // ring of per-group activation sums in shared memory
+constexpr int kXSlotBytes = kTileT * 4;
 constexpr int kTmemCols = 512;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
@@ -69,7 +72,8 @@ struct Params {
     const float* xsum;     // [G, Mp] group sums of the rounded activations
     const float* inv;      // [Mp] 2^-e_m
     int M, N, K, G, Mp;
-    int log2_spg;          // log2(gs / 16): MMA k-steps per group
+    int gs;                // group size
+    int spgs;              // 64-wide stages per group when gs >= 64 (else 1)
     unsigned* err;
 };
 
@@ -78,7 +82,8 @@ struct Geo {
     static constexpr int kCodeRowBytes = PACKED ? kChunk / 2 : kChunk;    // per stage
     static constexpr int kCodeBytes = kTileN * kCodeRowBytes;
     static constexpr int kStageBytes = kXhBytes + kCodeBytes;             // multiple of 1024
-    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kXOff = kStages * kStageBytes;
+    static constexpr int kBarOff = kXOff + kXSlots * kXSlotBytes;
     static constexpr int kSmemBytes = 1024 + kBarOff + 512;
 };
 
@@ -89,6 +94,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared without a cache hint (data many CTAs read).
+__device__ __forceinline__ void bulk_g2s_nohint(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
 
@@ -258,7 +273,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restr
 }
 
 // ------------------------------------------------------------- main kernel
-template <bool PACKED>
+// GK: MMA k-steps (16 wide) per group when a group fits in one stage
+// (gs = 16 -> 1, gs = 32 -> 2), or 4 when a group spans whole stages (gs >= 64).
+template <bool PACKED, int GK>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_x,
                const Params p) {
@@ -272,10 +289,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto empty = [&](int i) { return bars + 8u * (kStages + i); };
     auto a_full = [&](int i) { return bars + 8u * (2 * kStages + i); };
     auto a_empty = [&](int i) { return bars + 8u * (2 * kStages + kABufs + i); };
-    auto p_full = [&](int i) { return bars + 8u * (2 * kStages + 2 * kABufs + i); };
-    auto p_empty = [&](int i) { return bars + 8u * (2 * kStages + 2 * kABufs + 2 + i); };
-    const uint32_t done_bar = bars + 8u * (2 * kStages + 2 * kABufs + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + 8 * (2 * kStages + 2 * kABufs + 5));
+    constexpr int kPB = 2 * kStages + 2 * kABufs;   // first P barrier
+    constexpr int kXB = kPB + 2 * kPBufs;            // first activation-sum barrier
+    constexpr int kDone = kXB + 2 * kXSlots;
+    auto p_full = [&](int i) { return bars + 8u * (kPB + i); };
+    auto p_empty = [&](int i) { return bars + 8u * (kPB + kPBufs + i); };
+    auto x_full = [&](int i) { return bars + 8u * (kXB + i); };
+    auto x_empty = [&](int i) { return bars + 8u * (kXB + kXSlots + i); };
+    const uint32_t done_bar = bars + 8u * kDone;
+    static_assert(8 * (kDone + 1) + 4 <= 512, "barrier area");
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + 8 * (kDone + 1));
+    const uint32_t xring = base + Gm::kXOff;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -293,9 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(a_full(i), 128);
             mbar_init(a_empty(i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kPBufs; ++i) {
             mbar_init(p_full(i), 1);
             mbar_init(p_empty(i), 256);
+        }
+        for (int i = 0; i < kXSlots; ++i) {
+            mbar_init(x_full(i), 1);
+            mbar_init(x_empty(i), 256);
         }
         mbar_init(done_bar, 1);
         fence_mbar_init();
@@ -317,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&map_q);
             prefetch_tmap(&map_x);
-            int issued = 0;
-            for (int i = 0; i < nstages; ++i) {
+            int issued = 0, xissued = 0;
+            bool dead = false;
+            for (int i = 0; i < nstages && !dead; ++i) {
                 const int st = i % kStages;
                 if (i >= kStages && !mbar_wait(empty(st), ((i / kStages) & 1) ^ 1)) {
                     report_error(p.err, DEVERR_TC_WAIT);
@@ -329,41 +358,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(sb, &map_x, i * kChunk, m0, full(st));
                 tma_load_2d(sb + kXhBytes, &map_q, i * Gm::kCodeRowBytes, n0, full(st));
                 issued = i + 1;
+                // Activation sums of the groups that start inside this chunk.
+                const int ke = min(p.K, (i + 1) * kChunk);
+                for (int j = xissued; j * p.gs < ke; ++j) {
+                    const int sl = j % kXSlots;
+                    if (j >= kXSlots && !mbar_wait(x_empty(sl), ((j / kXSlots) & 1) ^ 1)) {
+                        report_error(p.err, DEVERR_TC_WAIT);
+                        dead = true;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(x_full(sl), kXSlotBytes);
+                    bulk_g2s_nohint(xring + sl * kXSlotBytes, p.xsum + (size_t)j * p.Mp + m0,
+                                    kXSlotBytes, x_full(sl));
+                    xissued = j + 1;
+                }
             }
             // Copies must land before the CTA can exit, whatever happened above.
             for (int i = max(0, issued - kStages); i < issued; ++i)
                 if (!mbar_wait(full(i % kStages), (i / kStages) & 1))
                     report_error(p.err, DEVERR_WAIT_DRAIN);
+            for (int j = max(0, xissued - kXSlots); j < xissued; ++j)
+                if (!mbar_wait(x_full(j % kXSlots), (j / kXSlots) & 1))
+                    report_error(p.err, DEVERR_WAIT_DRAIN);
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
+        // The issue loop is kept lean (ring indices and phase bits carried in
+        // counters, k-steps unrolled): every instruction between two MMAs
+        // of the single issuing thread delays the tensor pipe.
         if (lane == 0) {
-            const int spg_mask = (1 << p.log2_spg) - 1;
-            for (int ks = 0; ks < nks; ++ks) {
-                const int i = ks >> 2, kk = ks & 3;
-                const int j = ks >> p.log2_spg;
-                const bool first = (ks & spg_mask) == 0;
-                const bool last = (ks & spg_mask) == spg_mask;
-                if (kk == 0) {
-                    if (!mbar_wait(full(i % kStages), (i / kStages) & 1) ||
-                        !mbar_wait(a_full(i % kABufs), (i / kABufs) & 1)) {
-                        report_error(p.err, DEVERR_TC_WAIT);
-                        break;
-                    }
-                }
-                if (first && j >= 2 && !mbar_wait(p_empty(j & 1), ((j >> 1) & 1) ^ 1)) {
+            int st = 0, ab = 0, pb = 0, gst = 0, groups = 0;
+            uint32_t fph = 0, aph = 0, pph = 0;
+            bool dead = false;
+            for (int i = 0; i < nstages && !dead; ++i) {
+                const int nk = min(4, nks - 4 * i);
+                if (!mbar_wait(full(st), fph) || !mbar_wait(a_full(ab), aph)) {
                     report_error(p.err, DEVERR_TC_WAIT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = base + (i % kStages) * Gm::kStageBytes;
-                tc_mma_ts(tmem + (j & 1) * kPCols, tmem + kACol0 + (i % kABufs) * 32 + kk * 8,
-                          sw128_desc(sb + kk * 32), kIdesc, first ? 0u : 1u);
-                if (last) tc_commit(p_full(j & 1));
-                if (kk == 3 || ks == nks - 1) {
-                    tc_commit(empty(i % kStages));
-                    tc_commit(a_empty(i % kABufs));
+                const uint32_t sb = base + st * Gm::kStageBytes;
+                const uint32_t aa = tmem + kACol0 + ab * 32;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    if (GK < 4 && kk >= nk) break;
+                    const bool gstart = (GK == 4) ? (kk == 0 && gst == 0) : (kk % GK == 0);
+                    if (gstart && groups >= kPBufs) {
+                        if (!mbar_wait(p_empty(pb), pph ^ 1)) {
+                            report_error(p.err, DEVERR_TC_WAIT);
+                            dead = true;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    tc_mma_ts(tmem + pb * kPCols, aa + kk * 8, sw128_desc(sb + kk * 32), kIdesc,
+                              gstart ? 0u : 1u);
+                    const bool gend =
+                        (GK == 4) ? (kk == 3 && gst == p.spgs - 1) : (kk % GK == GK - 1);
+                    if (gend) {
+                        tc_commit(p_full(pb));
+                        ++groups;
+                        if (++pb == kPBufs) { pb = 0; pph ^= 1; }
+                    }
                 }
+                tc_commit(empty(st));
+                tc_commit(a_empty(ab));
+                if (++st == kStages) { st = 0; fph ^= 1; }
+                if (++ab == kABufs) { ab = 0; aph ^= 1; }
+                if (GK == 4 && ++gst == p.spgs) gst = 0;
             }
             tc_commit(done_bar);
             if (!mbar_wait(done_bar, 0)) report_error(p.err, DEVERR_WAIT_DRAIN);
@@ -372,10 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- converters
         const int row = threadIdx.x;  // 0..127: lane 32*warp + lane of tensor memory
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        int st = 0, ab = 0;
+        uint32_t fph = 0, aph = 0;
         for (int i = 0; i < nstages; ++i) {
-            const int st = i % kStages, ab = i % kABufs;
-            if (!warp_wait(full(st), (i / kStages) & 1) ||
-                (i >= kABufs && !warp_wait(a_empty(ab), ((i / kABufs) & 1) ^ 1))) {
+            if (!warp_wait(full(st), fph) || (i >= kABufs && !warp_wait(a_empty(ab), aph ^ 1))) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
                 break;
             }
@@ -416,6 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(a_full(ab));
+            if (++st == kStages) { st = 0; fph ^= 1; }
+            if (++ab == kABufs) { ab = 0; aph ^= 1; }
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------ epilogue
@@ -431,38 +495,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const float* srow = p.scales + (size_t)(nvalid ? n : 0) * p.G;
         const float* brow = p.biases + (size_t)(nvalid ? n : 0) * p.G;
+        int pb = 0, xsl = 0;
+        uint32_t pph = 0, xph = 0;
         for (int j = 0; j < p.G; ++j) {
-            const int pb = j & 1;
             const float s = nvalid ? __ldg(srow + j) : 0.f;
             const float b = nvalid ? __ldg(brow + j) : 0.f;
             const float2 s2 = make_float2(s, s), b2 = make_float2(b, b);
-            const float4* xs = reinterpret_cast<const float4*>(p.xsum + (size_t)j * p.Mp + t0);
-            if (!warp_wait(p_full(pb), (j >> 1) & 1)) {
+            if (!warp_wait(p_full(pb), pph) || !warp_wait(x_full(xsl), xph)) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const float4* xs =
+                reinterpret_cast<const float4*>(smem + Gm::kXOff + xsl * kXSlotBytes) + half * 16;
 #pragma unroll
             for (int hf = 0; hf < 4; ++hf) {
+                float4 xv[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[hf * 4 + c4];
                 uint32_t r[16];
                 tmem_ld16(tmem + lane_base + pb * kPCols + half * 64 + hf * 16, r);
-                if (hf == 3) {
+                if (hf == 3) {  // everything of group j is read: release P and the sums
                     tc_fence_before();
                     mbar_arrive(p_empty(pb));
+                    mbar_arrive(x_empty(xsl));
                 }
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    const float4 xv = __ldg(xs + hf * 4 + c4);
                     const int c = hf * 8 + c4 * 2;
-                    float2 t = __ffma2_rn(b2, make_float2(xv.x, xv.y), acc[c]);
+                    float2 t = __ffma2_rn(b2, make_float2(xv[c4].x, xv[c4].y), acc[c]);
                     acc[c] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4]),
                                                         __uint_as_float(r[4 * c4 + 1])), t);
-                    t = __ffma2_rn(b2, make_float2(xv.z, xv.w), acc[c + 1]);
+                    t = __ffma2_rn(b2, make_float2(xv[c4].z, xv[c4].w), acc[c + 1]);
                     acc[c + 1] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4 + 2]),
                                                             __uint_as_float(r[4 * c4 + 3])), t);
                 }
             }
+            if (++pb == kPBufs) { pb = 0; pph ^= 1; }
+            if (++xsl == kXSlots) { xsl = 0; xph ^= 1; }
         }
         if (ok) {
             // Lane l holds 2^-e of activation rows t0 + 2l and t0 + 2l + 1.
@@ -529,12 +600,12 @@ Layout layout(const GemvArgs& a) {
     return L;
 }
 
-template <bool PACKED>
+template <bool PACKED, int GK>
 int launch_main(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx, const Params& kp,
                 dim3 grid, cudaStream_t s) {
     constexpr int smem = Geo<PACKED>::kSmemBytes;
     static int configured[64] = {0};
-    auto kern = mma_kernel<PACKED>;
+    auto kern = mma_kernel<PACKED, GK>;
     if (dc.device >= 0 && dc.device < 64 && !configured[dc.device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -615,13 +686,18 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
     kp.K = (int)a.K;
     kp.G = L.G;
     kp.Mp = L.Mp;
-    int l = 0;
-    while ((16 << l) < a.gs) ++l;
-    kp.log2_spg = l;
+    kp.gs = a.gs;
+    kp.spgs = a.gs >= kChunk ? a.gs / kChunk : 1;
     kp.err = dc.err;
     const dim3 grid(L.Mp / kTileT, (unsigned)((a.N + kTileN - 1) / kTileN));
-    return packed ? launch_main<true>(dc, mq, mx, kp, grid, s)
-                  : launch_main<false>(dc, mq, mx, kp, grid, s);
+    if (a.gs == 16)
+        return packed ? launch_main<true, 1>(dc, mq, mx, kp, grid, s)
+                      : launch_main<false, 1>(dc, mq, mx, kp, grid, s);
+    if (a.gs == 32)
+        return packed ? launch_main<true, 2>(dc, mq, mx, kp, grid, s)
+                      : launch_main<false, 2>(dc, mq, mx, kp, grid, s);
+    return packed ? launch_main<true, 4>(dc, mq, mx, kp, grid, s)
+                  : launch_main<false, 4>(dc, mq, mx, kp, grid, s);
 }
 
 }  // namespace qg
