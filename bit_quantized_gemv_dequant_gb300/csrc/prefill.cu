@@ -56,7 +56,7 @@ constexpr int kABufs = 4;      // A operand buffers in tensor memory (32 columns
 constexpr int kPBufs = 3;      // P_g accumulators in tensor memory
 constexpr int kPCols = kTileT; // columns per P buffer
 constexpr int kACol0 = kPBufs * kPCols;  // A buffers follow: 384 + 4 * 32 = 512 columns
-constexpr int kXSlots = 8;     // ring of per-group activation sums in shared memory
+constexpr int kXSlots = 32;    // ring of per-group activation sums in shared memory
 constexpr int kXSlotBytes = kTileT * 4;
 constexpr int kTmemCols = 512;
 constexpr int kProducerWarp = 12;
@@ -66,8 +66,8 @@ constexpr int kXhBytes = kTileT * kChunk * 2;  // 16 KB per stage
 constexpr int kPrepThreads = 256;
 
 struct Params {
-    const float* scales;   // [N, G]
-    const float* biases;   // [N, G]
+    const float* scales_t; // [G, N] (scales transposed by the prep kernel)
+    const float* biases_t; // [G, N]
     float* y;              // [M, N]
     const float* xsum;     // [G, Mp] group sums of the rounded activations
     const float* inv;      // [Mp] 2^-e_m
@@ -84,7 +84,7 @@ struct Geo {
     static constexpr int kStageBytes = kXhBytes + kCodeBytes;             // multiple of 1024
     static constexpr int kXOff = kStages * kStageBytes;
     static constexpr int kBarOff = kXOff + kXSlots * kXSlotBytes;
-    static constexpr int kSmemBytes = 1024 + kBarOff + 512;
+    static constexpr int kSmemBytes = 1024 + kBarOff + 1024;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -151,6 +151,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
+// Issue a 16-column load without waiting; tmem_wait16 completes it. The
+// registers pass through the wait as read-write operands, so no use of them
+// can be scheduled between the two.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -191,15 +214,40 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ------------------------------------------------------------- prep kernel
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const float* __restrict__ x,
-                                                            __half* __restrict__ xh,
-                                                            float* __restrict__ xsum,
-                                                            float* __restrict__ inv, int M, int K,
-                                                            int gs, int G, int Mp) {
+// Blocks [0, Mp) prepare activation rows; blocks [Mp, Mp + tiles) transpose
+// 32 x 32 tiles of the scales and biases to [G, N], so that the main
+// kernel's epilogue (one weight row per thread) reads them coalesced.
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(
+    const float* __restrict__ x, __half* __restrict__ xh, float* __restrict__ xsum,
+    float* __restrict__ inv, const float* __restrict__ sc, const float* __restrict__ bi,
+    float* __restrict__ sc_t, float* __restrict__ bi_t, int M, int N, int K, int gs, int G,
+    int Mp) {
     __shared__ float red[kPrepThreads / 32];
     __shared__ float amax_s;
-    const int m = blockIdx.x;
+    __shared__ float tile[2][32][33];
     const int t = threadIdx.x;
+    if ((int)blockIdx.x >= Mp) {
+        const int tiles_g = (G + 31) / 32;
+        const int tb = blockIdx.x - Mp;
+        const int n_0 = (tb / tiles_g) * 32, g_0 = (tb % tiles_g) * 32;
+        const int tx = t & 31, ty = t >> 5;  // 32 x 8 threads
+        for (int r = ty; r < 32; r += 8) {
+            const int n = n_0 + r, g = g_0 + tx;
+            const bool in = n < N && g < G;
+            tile[0][r][tx] = in ? __ldg(sc + (size_t)n * G + g) : 0.f;
+            tile[1][r][tx] = in ? __ldg(bi + (size_t)n * G + g) : 0.f;
+        }
+        __syncthreads();
+        for (int r = ty; r < 32; r += 8) {
+            const int g = g_0 + r, n = n_0 + tx;
+            if (g < G && n < N) {
+                sc_t[(size_t)g * N + n] = tile[0][tx][r];
+                bi_t[(size_t)g * N + n] = tile[1][tx][r];
+            }
+        }
+        return;
+    }
+    const int m = blockIdx.x;
     const int lane = t & 31, warp = t >> 5;
     if (m >= M) {  // padding rows: zero group sums so the epilogue reads defined values
         for (int g = t; g < G; g += kPrepThreads) xsum[(size_t)g * Mp + m] = 0.f;
@@ -297,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto x_full = [&](int i) { return bars + 8u * (kXB + i); };
     auto x_empty = [&](int i) { return bars + 8u * (kXB + kXSlots + i); };
     const uint32_t done_bar = bars + 8u * kDone;
-    static_assert(8 * (kDone + 1) + 4 <= 512, "barrier area");
+    static_assert(8 * (kDone + 1) + 4 <= 1024, "barrier area");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + 8 * (kDone + 1));
     const uint32_t xring = base + Gm::kXOff;
 
@@ -388,11 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of the single issuing thread delays the tensor pipe.
         if (lane == 0) {
             int st = 0, ab = 0, pb = 0, gst = 0, groups = 0;
-            uint32_t fph = 0, aph = 0, pph = 0;
+            uint32_t aph = 0, pph = 0;
             bool dead = false;
             for (int i = 0; i < nstages && !dead; ++i) {
                 const int nk = min(4, nks - 4 * i);
-                if (!mbar_wait(full(st), fph) || !mbar_wait(a_full(ab), aph)) {
+                // a_full implies the stage's copies landed (the converters waited for
+                // them) and, for groups of 64 or more, that the P buffers the stage
+                // starts are free (the converters waited for those too): one barrier
+                // poll per stage, since each poll stalls the issuing thread.
+                if (!mbar_wait(a_full(ab), aph)) {
                     report_error(p.err, DEVERR_TC_WAIT);
                     break;
                 }
@@ -403,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 4; ++kk) {
                     if (GK < 4 && kk >= nk) break;
                     const bool gstart = (GK == 4) ? (kk == 0 && gst == 0) : (kk % GK == 0);
-                    if (gstart && groups >= kPBufs) {
+                    if (GK < 4 && gstart && groups >= kPBufs) {
                         if (!mbar_wait(p_empty(pb), pph ^ 1)) {
                             report_error(p.err, DEVERR_TC_WAIT);
                             dead = true;
@@ -423,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(empty(st));
                 tc_commit(a_empty(ab));
-                if (++st == kStages) { st = 0; fph ^= 1; }
+                if (++st == kStages) st = 0;
                 if (++ab == kABufs) { ab = 0; aph ^= 1; }
                 if (GK == 4 && ++gst == p.spgs) gst = 0;
             }
@@ -434,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- converters
         const int row = threadIdx.x;  // 0..127: lane 32*warp + lane of tensor memory
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        int st = 0, ab = 0;
-        uint32_t fph = 0, aph = 0;
+        int st = 0, ab = 0, gst = 0, groups = 0, pb = 0;
+        uint32_t fph = 0, aph = 0, pph = 0;
         for (int i = 0; i < nstages; ++i) {
             if (!warp_wait(full(st), fph) || (i >= kABufs && !warp_wait(a_empty(ab), aph ^ 1))) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
@@ -476,10 +528,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st16(acol + hf * 16, h);
             }
             tmem_st_wait();
+            if (GK == 4 && gst == 0) {
+                // This stage starts a group: its P buffer must be drained first.
+                if (groups >= kPBufs && !warp_wait(p_empty(pb), pph ^ 1)) {
+                    if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
+                    break;
+                }
+                ++groups;
+                if (++pb == kPBufs) { pb = 0; pph ^= 1; }
+            }
             tc_fence_before();
             mbar_arrive(a_full(ab));
             if (++st == kStages) { st = 0; fph ^= 1; }
             if (++ab == kABufs) { ab = 0; aph ^= 1; }
+            if (GK == 4 && ++gst == p.spgs) gst = 0;
         }
     } else if (warp < 12) {
         // ------------------------------------------------------------ epilogue
@@ -493,14 +555,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.f, 0.f);
         bool ok = true;
-        const float* srow = p.scales + (size_t)(nvalid ? n : 0) * p.G;
-        const float* brow = p.biases + (size_t)(nvalid ? n : 0) * p.G;
+        // Column n of the transposed scales/biases: a warp's loads are coalesced.
+        const float* srow = p.scales_t + (nvalid ? n : 0);
+        const float* brow = p.biases_t + (nvalid ? n : 0);
         int pb = 0, xsl = 0;
         uint32_t pph = 0, xph = 0;
+        // Scale and bias of the next group are loaded one group ahead.
+        float s_nx = nvalid ? __ldg(srow) : 0.f;
+        float b_nx = nvalid ? __ldg(brow) : 0.f;
+        // acc[c] (tokens 2c, 2c+1 of this warp's 64) += s * P + b * X for one
+        // 16-column chunk hf of P.
+        auto fma_chunk = [&](int hf, const uint32_t (&r)[16], const float4 (&xv)[4], float2 s2,
+                             float2 b2) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int c = hf * 8 + c4 * 2;
+                float2 t = __ffma2_rn(b2, make_float2(xv[c4].x, xv[c4].y), acc[c]);
+                acc[c] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4]),
+                                                    __uint_as_float(r[4 * c4 + 1])), t);
+                t = __ffma2_rn(b2, make_float2(xv[c4].z, xv[c4].w), acc[c + 1]);
+                acc[c + 1] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4 + 2]),
+                                                        __uint_as_float(r[4 * c4 + 3])), t);
+            }
+        };
         for (int j = 0; j < p.G; ++j) {
-            const float s = nvalid ? __ldg(srow + j) : 0.f;
-            const float b = nvalid ? __ldg(brow + j) : 0.f;
-            const float2 s2 = make_float2(s, s), b2 = make_float2(b, b);
+            const float2 s2 = make_float2(s_nx, s_nx), b2 = make_float2(b_nx, b_nx);
+            if (nvalid && j + 1 < p.G) {
+                s_nx = __ldg(srow + (size_t)(j + 1) * p.N);
+                b_nx = __ldg(brow + (size_t)(j + 1) * p.N);
+            }
             if (!warp_wait(p_full(pb), pph) || !warp_wait(x_full(xsl), xph)) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
                 ok = false;
@@ -509,29 +592,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float4* xs =
                 reinterpret_cast<const float4*>(smem + Gm::kXOff + xsl * kXSlotBytes) + half * 16;
+            const uint32_t pcol = tmem + lane_base + pb * kPCols + half * 64;
+            // Four 16-column chunks; the load of chunk hf+1 is in flight while
+            // chunk hf is multiplied.
+            uint32_t ra[16], rb[16];
+            float4 xv[4];
+            tmem_ld16_async(pcol, ra);
+            tmem_wait16(ra);
 #pragma unroll
-            for (int hf = 0; hf < 4; ++hf) {
-                float4 xv[4];
+            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[c4];
+            tmem_ld16_async(pcol + 16, rb);
+            fma_chunk(0, ra, xv, s2, b2);
+            tmem_wait16(rb);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[hf * 4 + c4];
-                uint32_t r[16];
-                tmem_ld16(tmem + lane_base + pb * kPCols + half * 64 + hf * 16, r);
-                if (hf == 3) {  // everything of group j is read: release P and the sums
-                    tc_fence_before();
-                    mbar_arrive(p_empty(pb));
-                    mbar_arrive(x_empty(xsl));
-                }
+            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[4 + c4];
+            tmem_ld16_async(pcol + 32, ra);
+            fma_chunk(1, rb, xv, s2, b2);
+            tmem_wait16(ra);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int c = hf * 8 + c4 * 2;
-                    float2 t = __ffma2_rn(b2, make_float2(xv[c4].x, xv[c4].y), acc[c]);
-                    acc[c] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4]),
-                                                        __uint_as_float(r[4 * c4 + 1])), t);
-                    t = __ffma2_rn(b2, make_float2(xv[c4].z, xv[c4].w), acc[c + 1]);
-                    acc[c + 1] = __ffma2_rn(s2, make_float2(__uint_as_float(r[4 * c4 + 2]),
-                                                            __uint_as_float(r[4 * c4 + 3])), t);
-                }
-            }
+            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[8 + c4];
+            tmem_ld16_async(pcol + 48, rb);
+            fma_chunk(2, ra, xv, s2, b2);
+            tmem_wait16(rb);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[12 + c4];
+            // Everything of group j is read: release P and the sums.
+            tc_fence_before();
+            mbar_arrive(p_empty(pb));
+            mbar_arrive(x_empty(xsl));
+            fma_chunk(3, rb, xv, s2, b2);
             if (++pb == kPBufs) { pb = 0; pph ^= 1; }
             if (++xsl == kXSlots) { xsl = 0; xph ^= 1; }
         }
@@ -584,7 +673,7 @@ int encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 }
 
 struct Layout {
-    size_t xh, xsum, inv, total;
+    size_t xh, xsum, inv, sc_t, bi_t, total;
     int Mp, G;
 };
 
@@ -596,7 +685,9 @@ Layout layout(const GemvArgs& a) {
     L.xh = 0;
     L.xsum = up((size_t)a.M * a.K * 2);
     L.inv = L.xsum + up((size_t)L.G * L.Mp * 4);
-    L.total = L.inv + up((size_t)L.Mp * 4);
+    L.sc_t = L.inv + up((size_t)L.Mp * 4);
+    L.bi_t = L.sc_t + up((size_t)L.G * a.N * 4);
+    L.total = L.bi_t + up((size_t)L.G * a.N * 4);
     return L;
 }
 
@@ -671,13 +762,19 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
             return QG_ERR_UNSUPPORTED;
     }
 
-    prep_kernel<<<L.Mp, kPrepThreads, 0, s>>>(a.x, xh, xsum, inv, (int)a.M, (int)a.K, a.gs, L.G, L.Mp);
+    float* sc_t = reinterpret_cast<float*>(w8 + L.sc_t);
+    float* bi_t = reinterpret_cast<float*>(w8 + L.bi_t);
+    const long long tiles = ((a.N + 31) / 32) * (long long)((L.G + 31) / 32);
+    if (tiles > 0x7FFFFFFFll - L.Mp) return QG_ERR_UNSUPPORTED;
+    prep_kernel<<<(unsigned)(L.Mp + tiles), kPrepThreads, 0, s>>>(
+        a.x, xh, xsum, inv, a.scales, a.biases, sc_t, bi_t, (int)a.M, (int)a.N, (int)a.K, a.gs,
+        L.G, L.Mp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
 
     Params kp{};
-    kp.scales = a.scales;
-    kp.biases = a.biases;
+    kp.scales_t = sc_t;
+    kp.biases_t = bi_t;
     kp.y = a.y[0];
     kp.xsum = xsum;
     kp.inv = inv;
