@@ -38,6 +38,7 @@ if ROOT not in sys.path:
 METRIC = ("quantized GEMV effective HBM GB/s and % of GB300 peak at M=1/8; µs/call")
 L2_BYTES = 129 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 SM_COUNT_NOMINAL = 152
 
@@ -510,6 +511,7 @@ def main():
 
     barrier = dist.barrier if dist else None
     hbm_peak, peak_src, peak_doc = peaks()
+    tensor_peak = float(peak_doc.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     qg.set_option(qg.QG_OPT_PDL, args.pdl)
 
     # Headline: dual Q4_0, M = 1.
@@ -613,6 +615,12 @@ def main():
                 steps = args.sweep_steps if "512" not in name else max(20, args.sweep_steps // 20)
                 res = measure(r, steps, 5)
                 res["frac_of_hbm_peak"] = res["gbs"] / hbm_peak
+                if "512" in name:
+                    # tensor-core prefill: fp16 MMAs, compared with the measured dense
+                    # bf16 peak (fp16 and bf16 share one tensor-core rate)
+                    res["tflops"] = r.flops / (res["us_per_call"] * 1e6)
+                    res["frac_of_tensor_peak"] = res["tflops"] / tensor_peak
+                    res["tensor_peak_tflops"] = tensor_peak
                 sweep[name] = res
                 del r
                 torch.cuda.empty_cache()
