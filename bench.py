@@ -270,6 +270,30 @@ def make_qkv(seq=4096, qs=2048, ks=2048, vs=4096, case=4):
 
 
 # ------------------------------------------------------------------ timing
+def sweep_specs():
+    """(name, runner factory) for every configuration the sweep times."""
+    specs = [
+        ("cfg0 q4_0", lambda: make_single("q4_0", 1, 1024, 1024, 0)),
+        ("cfg2 q4_k N=4096", lambda: make_single("q4_k", 1, 4096, 4096, 2)),
+        ("cfg2 q4_k N=12288", lambda: make_single("q4_k", 1, 12288, 4096, 2)),
+        ("cfg3 affine u8 M=1", lambda: make_single("affine", 1, 4096, 4096, 3, 64, 0)),
+        ("cfg3 affine packed M=1", lambda: make_single("affine", 1, 4096, 4096, 3, 64, 1)),
+        ("cfg3 affine u8 M=8", lambda: make_single("affine", 8, 4096, 4096, 3, 64, 0)),
+        ("cfg3 affine packed M=8", lambda: make_single("affine", 8, 4096, 4096, 3, 64, 1)),
+        ("cfg3 affine u8 M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 0)),
+        ("cfg3 affine packed M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 1)),
+        ("cfg4 qkv_split", lambda: make_qkv()),
+    ]
+    for M in (1, 2, 4, 8):
+        specs += [
+            (f"cfg4 M={M} q+gate dual", lambda M=M: make_dual_q4_0(M, 4096, 4096, 40)),
+            (f"cfg4 M={M} k+v dual", lambda M=M: make_dual_q4_0(M, 1024, 4096, 50)),
+            (f"cfg4 M={M} ffn up q4_k", lambda M=M: make_single("q4_k", M, 12288, 4096, 60)),
+            (f"cfg4 M={M} ffn down q4_k", lambda M=M: make_single("q4_k", M, 4096, 12288, 70)),
+        ]
+    return specs
+
+
 def time_runner(r: Runner, steps: int, warmup: int, chunk: int = 1000):
     """Warm up eagerly, then replay `steps` calls from CUDA graphs (chunks of
     at most `chunk` calls), timed with events on the capture stream. Returns
@@ -484,6 +508,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep-steps", type=int, default=400)
+    ap.add_argument("--only", default=None, metavar="NAME",
+                    help="time one sweep configuration (e.g. 'cfg3 affine u8 M=512') for "
+                         "--steps calls and print its line; for profiling runs")
     ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
                     help="launch with programmatic dependent launch (weights are static)")
     args = ap.parse_args()
@@ -513,6 +540,18 @@ def main():
     hbm_peak, peak_src, peak_doc = peaks()
     tensor_peak = float(peak_doc.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     qg.set_option(qg.QG_OPT_PDL, args.pdl)
+
+    if args.only is not None:
+        specs = dict(sweep_specs())
+        if args.only not in specs:
+            ap.error(f"--only: unknown configuration {args.only!r}; one of {sorted(specs)}")
+        r = specs[args.only]()
+        res = measure(r, args.steps, args.warmup)
+        res["tflops"] = r.flops / (res["us_per_call"] * 1e6)
+        if qg.device_error():
+            raise RuntimeError("device error word set")
+        print(json.dumps({"only": args.only, **res}), flush=True)
+        return
 
     # Headline: dual Q4_0, M = 1.
     r1 = make_dual_q4_0(1)
@@ -590,25 +629,7 @@ def main():
         sweep = {}
         del r1, r8
         torch.cuda.empty_cache()
-        specs = [
-            ("cfg0 q4_0", lambda: make_single("q4_0", 1, 1024, 1024, 0)),
-            ("cfg2 q4_k N=4096", lambda: make_single("q4_k", 1, 4096, 4096, 2)),
-            ("cfg2 q4_k N=12288", lambda: make_single("q4_k", 1, 12288, 4096, 2)),
-            ("cfg3 affine u8 M=1", lambda: make_single("affine", 1, 4096, 4096, 3, 64, 0)),
-            ("cfg3 affine packed M=1", lambda: make_single("affine", 1, 4096, 4096, 3, 64, 1)),
-            ("cfg3 affine u8 M=8", lambda: make_single("affine", 8, 4096, 4096, 3, 64, 0)),
-            ("cfg3 affine packed M=8", lambda: make_single("affine", 8, 4096, 4096, 3, 64, 1)),
-            ("cfg3 affine u8 M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 0)),
-            ("cfg3 affine packed M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 1)),
-            ("cfg4 qkv_split", lambda: make_qkv()),
-        ]
-        for M in (1, 2, 4, 8):
-            specs += [
-                (f"cfg4 M={M} q+gate dual", lambda M=M: make_dual_q4_0(M, 4096, 4096, 40)),
-                (f"cfg4 M={M} k+v dual", lambda M=M: make_dual_q4_0(M, 1024, 4096, 50)),
-                (f"cfg4 M={M} ffn up q4_k", lambda M=M: make_single("q4_k", M, 12288, 4096, 60)),
-                (f"cfg4 M={M} ffn down q4_k", lambda M=M: make_single("q4_k", M, 4096, 12288, 70)),
-            ]
+        specs = sweep_specs()
         for name, mk in specs:
             try:
                 r = mk()
