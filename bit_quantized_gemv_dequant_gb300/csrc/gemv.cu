@@ -16,6 +16,7 @@
 #include <algorithm>
 
 #include "gemv_fast.cuh"
+#include "gemv_stream.cuh"
 #include "qg_internal.cuh"
 
 namespace qg {
@@ -285,6 +286,90 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     return pl;
 }
 
+// ----------------------------------------------------------- stream plan
+// The streaming kernel (gemv_stream.cuh) for Mc <= 2: eligibility depends on
+// the format, K, the group size and pointer alignment only, never on N or the
+// number of matrices.
+struct SPlan {
+    bool ok;
+    int MT, LPR, W, S, slot_bytes, sbl, xs_bytes, xsum_bytes, smem, grid, tpr, tasks_per_w;
+};
+
+SPlan make_stream_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x) {
+    SPlan sp{};
+    sp.ok = false;
+    const long long mode = launch_option(QG_OPT_STREAM);
+    if (Mc > 2 || mode == 0) return sp;
+    // Automatic: the formats for which it measured faster than the staged
+    // kernel on GB300 (Q4_K); 2 takes it for every eligible call.
+    if (mode == 1 && a.fmt != FMT_Q4_K) return sp;
+    const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
+    if (a.K % 256) return sp;
+    const long long U = a.K / 256;
+    int LPR = 1;
+    while (LPR < 32 && U % (2 * LPR) == 0) LPR *= 2;
+    if (LPR < 4) return sp;
+    for (int i = 0; i < a.nw; ++i)
+        if (!aligned16(a.w[i])) return sp;
+    if (!aligned16(x)) return sp;
+    if (affine && (a.gs < 32 || !aligned16(a.scales) || !aligned16(a.biases))) return sp;
+    const int RW = 32 / LPR;
+    const long long rb = row_bytes(a.fmt, a.K);
+    if (rb * RW >= (1ll << 31) || a.K > (1 << 24)) return sp;
+    sp.MT = Mc;
+    sp.LPR = LPR;
+    sp.tpr = (int)(U / LPR);
+    sp.tasks_per_w = (int)((a.N + RW - 1) / RW);
+    const bool sums = a.fmt != FMT_Q4_0;
+    sp.xs_bytes = (int)(sp.MT * U * 65 * 16);            // 64 float4 + 1 padding per unit
+    sp.xsum_bytes = sums ? (int)(sp.MT * U * 12 * 4) : 0;  // 8 sums + 4 padding per unit
+    const int UB = a.fmt == FMT_AFF_U8 ? 256 : a.fmt == FMT_AFF_PACKED ? 128 : 144;
+    sp.sbl = affine ? (a.gs == 32 ? 32 : 16) : 0;
+    sp.slot_bytes = 32 * UB + 64 * sp.sbl;
+    const long long fixed = (long long)sp.xs_bytes + sp.xsum_bytes + 128;
+    auto smem_of = [&](int W, int S) { return fixed + (long long)W * S * sp.slot_bytes; };
+    const long long co_budget = dc.smem_per_sm / 2 - dc.reserved_smem;
+    const int ow = (int)launch_option(QG_OPT_STREAM_WARPS), os = (int)launch_option(QG_OPT_STREAM_SLOTS);
+    int W = 0, S = 0;
+    if (ow > 0 || os > 0) {
+        const int w = ow > 0 ? ow : 8, s2 = os > 0 ? os : 2;
+        if (smem_of(w, s2) <= dc.max_smem_optin) {
+            W = w;
+            S = s2;
+        }
+    }
+    if (W == 0) {
+        // Two CTAs per SM when 8 warps with two slots each fit in half an SM;
+        // otherwise one CTA with the most slots (up to 4) that fit.
+        if (smem_of(8, 2) <= co_budget) {
+            W = 8;
+            S = 2;
+        } else {
+            for (int s2 = 4; s2 >= 2 && W == 0; --s2)
+                if (smem_of(8, s2) <= dc.max_smem_optin) {
+                    W = 8;
+                    S = s2;
+                }
+            for (int w = 4; w >= 1 && W == 0; w /= 2)
+                if (smem_of(w, 2) <= dc.max_smem_optin) {
+                    W = w;
+                    S = 2;
+                }
+        }
+    }
+    if (W == 0) return sp;
+    sp.W = W;
+    sp.S = S;
+    sp.smem = (int)smem_of(W, S);
+    // Two CTAs per SM when they fit (both of this launch; as they retire, the
+    // next launch's CTAs take their place and start streaming).
+    const long long total = (long long)sp.tasks_per_w * a.nw;
+    const int per_sm = (sp.smem + dc.reserved_smem) * 2 <= dc.smem_per_sm ? 2 : 1;
+    sp.grid = (int)std::min<long long>(total, (long long)per_sm * dc.num_sms);
+    sp.ok = true;
+    return sp;
+}
+
 template <int FMT>
 int launch_general(const DevCtx& dc, const KParams& kp, cudaStream_t s) {
     const long long rows = (long long)kp.nw * kp.N;
@@ -296,6 +381,12 @@ int launch_general(const DevCtx& dc, const KParams& kp, cudaStream_t s) {
 
 }  // namespace
 
+int stream_launch_q4_0(const DevCtx&, const stream::Params&, int, int, int, int, int, bool, cudaStream_t);
+int stream_launch_q4_k(const DevCtx&, const stream::Params&, int, int, int, int, int, bool, cudaStream_t);
+int stream_launch_aff_u8(const DevCtx&, const stream::Params&, int, int, int, int, int, bool,
+                         cudaStream_t);
+int stream_launch_aff_packed(const DevCtx&, const stream::Params&, int, int, int, int, int, bool,
+                             cudaStream_t);
 int fast_launch_q4_0(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
 int fast_launch_q4_k(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
 int fast_launch_aff_u8(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
@@ -320,8 +411,55 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
         const float* x = a.x + m0 * a.K;
         float* y0 = a.y[0] + m0 * a.N;
         float* y1 = (a.nw > 1 ? a.y[1] : a.y[0]) + m0 * a.N;
-        const Plan pl = make_plan(dc, a, Mc);
         int rc;
+        const SPlan sp = make_stream_plan(dc, a, Mc, x);
+        if (sp.ok) {
+            stream::Params kp{};
+            kp.w[0] = a.w[0];
+            kp.w[1] = a.nw > 1 ? a.w[1] : a.w[0];
+            kp.out[0] = y0;
+            kp.out[1] = y1;
+            kp.x = x;
+            kp.s = a.scales;
+            kp.b = a.biases;
+            kp.M = Mc;
+            kp.N = (int)a.N;
+            kp.K = (int)a.K;
+            kp.nw = a.nw;
+            kp.tpr = sp.tpr;
+            kp.tpr_magic = sp.tpr > 1 ? (uint32_t)(((1ull << 32) + sp.tpr - 1) / sp.tpr) : 0u;
+            kp.tasks_per_w = sp.tasks_per_w;
+            kp.total_tasks = sp.tasks_per_w * a.nw;
+            kp.tasks_base = kp.total_tasks / sp.grid;
+            kp.tasks_rem = kp.total_tasks % sp.grid;
+            kp.S = sp.S;
+            kp.slot_bytes = sp.slot_bytes;
+            kp.sbl = sp.sbl;
+            kp.log2gs = affine ? ilog2(a.gs) : 0;
+            kp.G = affine ? (int)(a.K / a.gs) : 0;
+            kp.row_bytes = row_bytes(a.fmt, a.K);
+            kp.xs_bytes = sp.xs_bytes;
+            kp.xsum_bytes = sp.xsum_bytes;
+            kp.zero = 0u;
+            const bool pdl = launch_option(QG_OPT_PDL) != 0;
+            switch (a.fmt) {
+                case FMT_Q4_0:
+                    rc = stream_launch_q4_0(dc, kp, sp.MT, sp.LPR, sp.grid, sp.W, sp.smem, pdl, s);
+                    break;
+                case FMT_Q4_K:
+                    rc = stream_launch_q4_k(dc, kp, sp.MT, sp.LPR, sp.grid, sp.W, sp.smem, pdl, s);
+                    break;
+                case FMT_AFF_U8:
+                    rc = stream_launch_aff_u8(dc, kp, sp.MT, sp.LPR, sp.grid, sp.W, sp.smem, pdl, s);
+                    break;
+                default:
+                    rc = stream_launch_aff_packed(dc, kp, sp.MT, sp.LPR, sp.grid, sp.W, sp.smem, pdl, s);
+                    break;
+            }
+            if (rc != QG_OK) return rc;
+            continue;
+        }
+        const Plan pl = make_plan(dc, a, Mc);
         if (!pl.fast) {
             KParams kp{};
             kp.w[0] = a.w[0];
@@ -365,6 +503,8 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
         kp.units = pl.klen / geo(a.fmt).UE;
         kp.chunks_per_w = pl.stages_per_w;
         kp.total_chunks = pl.stages_per_w * a.nw;
+        kp.chunk_base = kp.total_chunks / pl.grid_x;
+        kp.chunk_rem = kp.total_chunks % pl.grid_x;
         kp.S = pl.S;
         kp.stage_bytes = pl.stage_bytes;
         kp.q_stride = pl.q_stride;

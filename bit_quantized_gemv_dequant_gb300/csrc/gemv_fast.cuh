@@ -124,6 +124,7 @@ struct Params {
     int nw;
     int klen, P, units;        // k-slice length, passes, units per row slice
     int chunks_per_w, total_chunks;
+    int chunk_base, chunk_rem;  // total_chunks = chunk_base * gridDim.x + chunk_rem
     int S, stage_bytes;
     int q_stride, sb_stride, sb_off;
     long long q_row_bytes;
@@ -295,8 +296,9 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
     const int lane = threadIdx.x & 31;
     const int ks = blockIdx.y;
     const int k0 = ks * p.klen;
-    const int c_begin = (int)((long long)p.total_chunks * blockIdx.x / gridDim.x);
-    const int c_end = (int)((long long)p.total_chunks * (blockIdx.x + 1) / gridDim.x);
+    // CTA b takes chunk_base chunks, plus one more when b < chunk_rem.
+    const int c_begin = (int)blockIdx.x * p.chunk_base + min((int)blockIdx.x, p.chunk_rem);
+    const int c_end = c_begin + p.chunk_base + ((int)blockIdx.x < p.chunk_rem ? 1 : 0);
     const int n_local = c_end - c_begin;
 
     if (threadIdx.x == 0) {

@@ -24,6 +24,9 @@ int g_ctx_rc[kMaxDevices];
 thread_local int t_last_cuda_error = 0;
 std::atomic<long long> g_opt_pdl{0};
 std::atomic<long long> g_opt_prefill_min_m{16};
+std::atomic<long long> g_opt_stream{1};
+std::atomic<long long> g_opt_stream_warps{0};
+std::atomic<long long> g_opt_stream_slots{0};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -142,6 +145,9 @@ long long launch_option(int option) {
     switch (option) {
         case QG_OPT_PDL: return g_opt_pdl.load(std::memory_order_relaxed);
         case QG_OPT_PREFILL_MIN_M: return g_opt_prefill_min_m.load(std::memory_order_relaxed);
+        case QG_OPT_STREAM: return g_opt_stream.load(std::memory_order_relaxed);
+        case QG_OPT_STREAM_WARPS: return g_opt_stream_warps.load(std::memory_order_relaxed);
+        case QG_OPT_STREAM_SLOTS: return g_opt_stream_slots.load(std::memory_order_relaxed);
         default: return 0;
     }
 }
@@ -318,6 +324,18 @@ int qg_set_option(int option, int64_t value) {
             if (value < 1) return QG_ERR_INVALID_ARG;
             g_opt_prefill_min_m.store(value, std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_STREAM:
+            if (value < 0 || value > 2) return QG_ERR_INVALID_ARG;
+            g_opt_stream.store(value, std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_STREAM_WARPS:
+            if (value < 0 || value > 8) return QG_ERR_INVALID_ARG;
+            g_opt_stream_warps.store(value, std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_STREAM_SLOTS:
+            if (value != 0 && (value < 2 || value > 8)) return QG_ERR_INVALID_ARG;
+            g_opt_stream_slots.store(value, std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }
@@ -328,6 +346,13 @@ int qg_get_option(int option, int64_t* value) {
         case QG_OPT_PDL: *value = g_opt_pdl.load(std::memory_order_relaxed); return QG_OK;
         case QG_OPT_PREFILL_MIN_M:
             *value = g_opt_prefill_min_m.load(std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_STREAM: *value = g_opt_stream.load(std::memory_order_relaxed); return QG_OK;
+        case QG_OPT_STREAM_WARPS:
+            *value = g_opt_stream_warps.load(std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_STREAM_SLOTS:
+            *value = g_opt_stream_slots.load(std::memory_order_relaxed);
             return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }

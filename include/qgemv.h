@@ -191,7 +191,23 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
 /*
  * QG_OPT_PREFILL_MIN_M (default 16, >= 1): smallest M for which qmm_affine
  * takes the tensor-core prefill path (when its other conditions hold). */
-enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2 };
+/*
+ * QG_OPT_STREAM (default 1): which GEMV/qmm calls with M <= 2 (per slice of
+ * x) take the streaming kernel instead of the staged-stage kernel. 0: none.
+ * 1: the formats for which it is the faster of the two (Q4_K). 2: every
+ * eligible call. Eligible: K % 256 == 0, (K / 256) % 4 == 0, the weight, x
+ * (and affine scale/bias) pointers 16-byte aligned and, for affine weights,
+ * group_size >= 32. Both kernels give results within the same tolerance; the
+ * choice never depends on N or on single versus dual calls, so the dual
+ * projection stays bitwise equal to two single projections under any
+ * setting.
+ *
+ * QG_OPT_STREAM_WARPS (default 0 = automatic; else 1..8) and
+ * QG_OPT_STREAM_SLOTS (default 0 = automatic; else 2..8): warps per CTA and
+ * shared-memory ring slots per warp of the streaming kernel (tuning). A
+ * setting whose shared memory does not fit falls back to the automatic one. */
+enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
+       QG_OPT_STREAM_SLOTS = 5 };
 QG_API int qg_set_option(int option, int64_t value);
 QG_API int qg_get_option(int option, int64_t* value);
 
