@@ -505,6 +505,9 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
         kp.total_chunks = pl.stages_per_w * a.nw;
         kp.chunk_base = kp.total_chunks / pl.grid_x;
         kp.chunk_rem = kp.total_chunks % pl.grid_x;
+        // The in-flight limit helps the bandwidth-bound M <= 2 calls; the
+        // compute-bound M >= 4 ones keep every stage in flight.
+        kp.ahead = pl.MT <= 2 ? std::min<int>((int)launch_option(QG_OPT_STAGES_AHEAD), pl.S) : 0;
         kp.S = pl.S;
         kp.stage_bytes = pl.stage_bytes;
         kp.q_stride = pl.q_stride;

@@ -125,6 +125,7 @@ struct Params {
     int klen, P, units;        // k-slice length, passes, units per row slice
     int chunks_per_w, total_chunks;
     int chunk_base, chunk_rem;  // total_chunks = chunk_base * gridDim.x + chunk_rem
+    int ahead;                  // chunks in flight at most (0: up to S)
     int S, stage_bytes;
     int q_stride, sb_stride, sb_off;
     long long q_row_bytes;
@@ -330,6 +331,18 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                 report_error(p.err, DEVERR_WAIT_EMPTY);
                 ok = false;
                 break;
+            }
+            // At most `ahead` chunks in flight: chunk i is requested once chunk
+            // i - ahead has landed, so that every SM's first chunks are not
+            // queued behind the whole grid's traffic (ahead <= S, so the
+            // awaited phase is the latest one of that stage).
+            if (p.ahead > 0 && i >= p.ahead) {
+                const int j = i - p.ahead;
+                if (!mbar_wait(smem_addr(&full[j % p.S]), (j / p.S) & 1)) {
+                    report_error(p.err, DEVERR_WAIT_FULL);
+                    ok = false;
+                    break;
+                }
             }
             const int cid = c_begin + i;
             const int wi = cid / p.chunks_per_w;

@@ -27,6 +27,7 @@ std::atomic<long long> g_opt_prefill_min_m{16};
 std::atomic<long long> g_opt_stream{1};
 std::atomic<long long> g_opt_stream_warps{0};
 std::atomic<long long> g_opt_stream_slots{0};
+std::atomic<long long> g_opt_ahead{2};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -148,6 +149,7 @@ long long launch_option(int option) {
         case QG_OPT_STREAM: return g_opt_stream.load(std::memory_order_relaxed);
         case QG_OPT_STREAM_WARPS: return g_opt_stream_warps.load(std::memory_order_relaxed);
         case QG_OPT_STREAM_SLOTS: return g_opt_stream_slots.load(std::memory_order_relaxed);
+        case QG_OPT_STAGES_AHEAD: return g_opt_ahead.load(std::memory_order_relaxed);
         default: return 0;
     }
 }
@@ -336,6 +338,10 @@ int qg_set_option(int option, int64_t value) {
             if (value != 0 && (value < 2 || value > 8)) return QG_ERR_INVALID_ARG;
             g_opt_stream_slots.store(value, std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_STAGES_AHEAD:
+            if (value < 0 || value > 64) return QG_ERR_INVALID_ARG;
+            g_opt_ahead.store(value, std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }
@@ -354,6 +360,7 @@ int qg_get_option(int option, int64_t* value) {
         case QG_OPT_STREAM_SLOTS:
             *value = g_opt_stream_slots.load(std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_STAGES_AHEAD: *value = g_opt_ahead.load(std::memory_order_relaxed); return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }

@@ -206,8 +206,14 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * QG_OPT_STREAM_SLOTS (default 0 = automatic; else 2..8): warps per CTA and
  * shared-memory ring slots per warp of the streaming kernel (tuning). A
  * setting whose shared memory does not fit falls back to the automatic one. */
+/*
+ * QG_OPT_STAGES_AHEAD (default 2; 0 = every stage of the ring; else 1..64):
+ * for M <= 2 (per slice of x) the staged-stage kernel requests weight chunk i
+ * only once chunk i - n has landed, so that each SM's first chunks are not
+ * queued behind the whole grid's traffic (tuning; a value above the ring size
+ * means the ring size). */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
-       QG_OPT_STREAM_SLOTS = 5 };
+       QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6 };
 QG_API int qg_set_option(int option, int64_t value);
 QG_API int qg_get_option(int option, int64_t* value);
 

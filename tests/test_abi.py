@@ -73,3 +73,30 @@ def test_validation_needs_no_gpu(lib):
     k = lib.qgemv_q4_k
     k.argtypes = [P, P, P, I64, I64, I64, P, C.c_size_t, P]
     assert k(fake, fake + 4096, fake + 8192, 1, 4, 128, None, 0, None) == 1  # K % 256
+
+
+def test_launch_options_round_trip_and_validation(lib):
+    """qg_set_option / qg_get_option need no GPU: values round-trip, and values
+    outside each option's documented range are refused."""
+    lib.qg_set_option.argtypes = [C.c_int, C.c_int64]
+    lib.qg_get_option.argtypes = [C.c_int, C.POINTER(C.c_int64)]
+    get = lambda o: (lambda v: (lib.qg_get_option(o, C.byref(v)), v.value))(C.c_int64())
+    cases = {1: ([0, 1], [2, -1]),            # QG_OPT_PDL
+             2: ([1, 64], [0]),               # QG_OPT_PREFILL_MIN_M
+             3: ([0, 1, 2], [3, -1]),         # QG_OPT_STREAM
+             4: ([0, 1, 8], [9, -1]),         # QG_OPT_STREAM_WARPS
+             5: ([0, 2, 8], [1, 9]),          # QG_OPT_STREAM_SLOTS
+             6: ([0, 1, 64], [65, -1])}       # QG_OPT_STAGES_AHEAD
+    for opt, (good, bad) in cases.items():
+        rc, old = get(opt)
+        assert rc == 0
+        try:
+            for v in good:
+                assert lib.qg_set_option(opt, v) == 0
+                assert get(opt) == (0, v)
+            for v in bad:
+                assert lib.qg_set_option(opt, v) == 1  # QG_ERR_INVALID_ARG
+                assert get(opt)[1] == good[-1]
+        finally:
+            assert lib.qg_set_option(opt, old) == 0
+    assert lib.qg_set_option(99, 0) == 1

@@ -274,3 +274,21 @@ def test_bounded_wait_reports_instead_of_hanging():
 
 def test_no_device_error_left():
     assert qg.device_error() == 0
+
+
+@pytest.mark.parametrize("ahead", [0, 1, 3])
+def test_stages_ahead_does_not_change_results(ahead):
+    """QG_OPT_STAGES_AHEAD only changes when chunks are requested, never the
+    arithmetic: results are bitwise equal to the default schedule."""
+    M, N, K = 1, 700, 4096
+    c = synth.q4_0_case(2300 + ahead, N, K, M, dual=True)
+    wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
+    base = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    old = qg.get_option(qg.QG_OPT_STAGES_AHEAD)
+    qg.set_option(qg.QG_OPT_STAGES_AHEAD, ahead)
+    try:
+        ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    finally:
+        qg.set_option(qg.QG_OPT_STAGES_AHEAD, old)
+    assert_bitwise(ya, base[0], f"ahead={ahead} y_a")
+    assert_bitwise(yb, base[1], f"ahead={ahead} y_b")
