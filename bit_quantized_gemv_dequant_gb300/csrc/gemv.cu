@@ -196,7 +196,7 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
     const FmtGeo g = geo(a.fmt);
     pl.MT = Mc <= 1 ? 1 : Mc <= 2 ? 2 : Mc <= 4 ? 4 : 8;
-    pl.W = pl.MT <= 2 ? 16 : 8;
+    pl.W = pl.MT <= 2 ? 16 : 12;
     if (a.K % g.UE) return pl;
     for (int i = 0; i < a.nw; ++i)
         if (!aligned16(a.w[i])) return pl;

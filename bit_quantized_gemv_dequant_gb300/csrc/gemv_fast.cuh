@@ -589,36 +589,38 @@ __global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params
                     }
 #pragma unroll
                 for (int w = 0; w < F::WORDS; ++w) {
-                    float4 xa[MT], xb[MT];
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        xa[m] = xp[(m * p.P * NCH + chunk_a<FMT>(w)) * 32];
-                        xb[m] = xp[(m * p.P * NCH + chunk_b<FMT>(w)) * 32];
-                    }
+                    // Decode the word of every row of the batch once, then stream x
+                    // row by row (only one x row's chunks live at a time; the
+                    // per-output arithmetic order is the same as x-major order).
+                    float2 f[RB][4];
 #pragma unroll
                     for (int b = 0; b < RB; ++b) {
                         const uint8_t* rowr = stg + (rb0 + b) * p.q_stride;
-                        float2 f[4];
                         if (FMT == FMT_Q4_0) {
                             decode_nibbles<FMT>(__funnelshift_rc(win[b][w], win[b][w + 1], qsh), mg,
-                                                cst, f);
+                                                cst, f[b]);
                         } else if (FMT == FMT_Q4_K || FMT == FMT_AFF_PACKED) {
                             const uint32_t v =
                                 *reinterpret_cast<const uint32_t*>(rowr + qo + 4 * w);
-                            decode_nibbles<FMT>(v, mg, cst, f);
+                            decode_nibbles<FMT>(v, mg, cst, f[b]);
                         } else {
                             const uint2 v = *reinterpret_cast<const uint2*>(rowr + qo + 8 * w);
-                            decode_bytes(v.x, v.y, mg, f);
+                            decode_bytes(v.x, v.y, mg, f[b]);
                         }
+                    }
 #pragma unroll
-                        for (int m = 0; m < MT; ++m) {
+                    for (int m = 0; m < MT; ++m) {
+                        const float4 xa = xp[(m * p.P * NCH + chunk_a<FMT>(w)) * 32];
+                        const float4 xb = xp[(m * p.P * NCH + chunk_b<FMT>(w)) * 32];
+#pragma unroll
+                        for (int b = 0; b < RB; ++b) {
                             if (FMT == FMT_Q4_K) {
-                                s_lo[m][b] = __ffma2_rn(f[0], make_float2(xa[m].x, xa[m].y), s_lo[m][b]);
-                                s_lo[m][b] = __ffma2_rn(f[1], make_float2(xa[m].z, xa[m].w), s_lo[m][b]);
-                                s_hi[m][b] = __ffma2_rn(f[2], make_float2(xb[m].x, xb[m].y), s_hi[m][b]);
-                                s_hi[m][b] = __ffma2_rn(f[3], make_float2(xb[m].z, xb[m].w), s_hi[m][b]);
+                                s_lo[m][b] = __ffma2_rn(f[b][0], make_float2(xa.x, xa.y), s_lo[m][b]);
+                                s_lo[m][b] = __ffma2_rn(f[b][1], make_float2(xa.z, xa.w), s_lo[m][b]);
+                                s_hi[m][b] = __ffma2_rn(f[b][2], make_float2(xb.x, xb.y), s_hi[m][b]);
+                                s_hi[m][b] = __ffma2_rn(f[b][3], make_float2(xb.z, xb.w), s_hi[m][b]);
                             } else {
-                                s_lo[m][b] = dot8(f, xa[m], xb[m], s_lo[m][b]);
+                                s_lo[m][b] = dot8(f[b], xa, xb, s_lo[m][b]);
                             }
                         }
                     }
@@ -733,7 +735,8 @@ namespace qg {
 namespace fast {
 
 // Largest rows-per-stage per (format, M bucket) that compiles without
-// register spills (16 consumer warps cap a thread at 96 registers, 8 at 168).
+// register spills (16 consumer warps + producer cap a thread at 96
+// registers; 12 + producer, used for M >= 4, at 128).
 __host__ __device__ constexpr int max_rows(int fmt, int MT) {
     return fmt == FMT_Q4_0   ? (MT == 1 ? 16 : MT == 8 ? 2 : 4)
            : fmt == FMT_Q4_K ? (MT == 1 ? 4 : MT == 8 ? 1 : 2)
@@ -741,7 +744,7 @@ __host__ __device__ constexpr int max_rows(int fmt, int MT) {
 }
 
 // (MT, R, GW) -> kernel instantiation: R rows per stage, shared by a group of
-// GW warps that split the passes. MT <= 2 runs 16 consumer warps, larger M 8.
+// GW warps that split the passes. MT <= 2 runs 16 consumer warps, larger M 12.
 template <int FMT, int MT, int W, int R>
 int dispatch_gw(const DevCtx& dc, const Params& kp, int GW, int grid, int smem, bool pdl,
                 cudaStream_t s) {
@@ -769,12 +772,12 @@ int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int grid
             if (R <= 2) return dispatch_gw<FMT, 2, 16, 2>(dc, kp, GW, grid, smem, pdl, s);
             return dispatch_gw<FMT, 2, 16, 4>(dc, kp, GW, grid, smem, pdl, s);
         case 4:
-            if (R <= 2) return dispatch_gw<FMT, 4, 8, 2>(dc, kp, GW, grid, smem, pdl, s);
-            return dispatch_gw<FMT, 4, 8, 4>(dc, kp, GW, grid, smem, pdl, s);
+            if (R <= 2) return dispatch_gw<FMT, 4, 12, 2>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 4, 12, 4>(dc, kp, GW, grid, smem, pdl, s);
         default:
-            if (R <= 1) return dispatch_gw<FMT, 8, 8, 1>(dc, kp, GW, grid, smem, pdl, s);
-            if (R == 2) return dispatch_gw<FMT, 8, 8, 2>(dc, kp, GW, grid, smem, pdl, s);
-            return dispatch_gw<FMT, 8, 8, 4>(dc, kp, GW, grid, smem, pdl, s);
+            if (R <= 1) return dispatch_gw<FMT, 8, 12, 1>(dc, kp, GW, grid, smem, pdl, s);
+            if (R == 2) return dispatch_gw<FMT, 8, 12, 2>(dc, kp, GW, grid, smem, pdl, s);
+            return dispatch_gw<FMT, 8, 12, 4>(dc, kp, GW, grid, smem, pdl, s);
     }
 }
 
