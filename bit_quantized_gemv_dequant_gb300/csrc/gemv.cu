@@ -197,6 +197,10 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     const FmtGeo g = geo(a.fmt);
     pl.MT = Mc <= 1 ? 1 : Mc <= 2 ? 2 : Mc <= 4 ? 4 : 8;
     pl.W = pl.MT <= 2 ? 16 : 12;
+    // Eight consumer warps (two CTAs per SM: this launch's and the next one's)
+    // when requested; M = 1 only.
+    const bool w8 = pl.MT == 1 && launch_option(QG_OPT_STAGED_WARPS) == 8;
+    if (w8) pl.W = 8;
     if (a.K % g.UE) return pl;
     for (int i = 0; i < a.nw; ++i)
         if (!aligned16(a.w[i])) return pl;
@@ -237,9 +241,10 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     for (int ri = 0; ri < nr; ++ri) {
         const int R = ropt[ri];
         if (R > fast::max_rows(a.fmt, pl.MT)) continue;
+        if (w8 && R < 4) continue;
         const int V = pl.MT * R;
         const int sums = g.sums ? pl.MT * pl.P * 32 * g.nh : 0;
-        for (int co = 1; co >= 0; --co) {
+        for (int co = 1; co >= (w8 ? 1 : 0); --co) {
             const int stage = ((R * pl.q_stride + 2 * R * pl.sb_stride + 16) + 127) & ~127;
             const int budget = co ? co_budget : dc.max_smem_optin;
             // Per stage: the copy, two mbarriers, an arrival counter and the
@@ -387,11 +392,14 @@ int stream_launch_aff_u8(const DevCtx&, const stream::Params&, int, int, int, in
                          cudaStream_t);
 int stream_launch_aff_packed(const DevCtx&, const stream::Params&, int, int, int, int, int, bool,
                              cudaStream_t);
-int fast_launch_q4_0(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
-int fast_launch_q4_k(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
-int fast_launch_aff_u8(const DevCtx&, const fast::Params&, int, int, int, int, int, bool, cudaStream_t);
-int fast_launch_aff_packed(const DevCtx&, const fast::Params&, int, int, int, int, int, bool,
-                           cudaStream_t);
+int fast_launch_q4_0(const DevCtx&, const fast::Params&, int, int, int, int, int, int, bool,
+                      cudaStream_t);
+int fast_launch_q4_k(const DevCtx&, const fast::Params&, int, int, int, int, int, int, bool,
+                      cudaStream_t);
+int fast_launch_aff_u8(const DevCtx&, const fast::Params&, int, int, int, int, int, int, bool,
+                      cudaStream_t);
+int fast_launch_aff_packed(const DevCtx&, const fast::Params&, int, int, int, int, int, int,
+                           bool, cudaStream_t);
 
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a) {
     size_t worst = 0;
@@ -528,16 +536,16 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
         const bool pdl = launch_option(QG_OPT_PDL) != 0;
         switch (a.fmt) {
             case FMT_Q4_0:
-                rc = fast_launch_q4_0(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                rc = fast_launch_q4_0(dc, kp, pl.MT, pl.R, pl.GW, pl.W, pl.grid_x, pl.smem, pdl, s);
                 break;
             case FMT_Q4_K:
-                rc = fast_launch_q4_k(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                rc = fast_launch_q4_k(dc, kp, pl.MT, pl.R, pl.GW, pl.W, pl.grid_x, pl.smem, pdl, s);
                 break;
             case FMT_AFF_U8:
-                rc = fast_launch_aff_u8(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                rc = fast_launch_aff_u8(dc, kp, pl.MT, pl.R, pl.GW, pl.W, pl.grid_x, pl.smem, pdl, s);
                 break;
             default:
-                rc = fast_launch_aff_packed(dc, kp, pl.MT, pl.R, pl.GW, pl.grid_x, pl.smem, pdl, s);
+                rc = fast_launch_aff_packed(dc, kp, pl.MT, pl.R, pl.GW, pl.W, pl.grid_x, pl.smem, pdl, s);
                 break;
         }
         if (rc != QG_OK) return rc;

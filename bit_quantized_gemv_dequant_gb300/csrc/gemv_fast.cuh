@@ -275,7 +275,7 @@ __device__ __forceinline__ void butterfly(float (&v)[V], int lane) {
 }
 
 template <int FMT, int MT, int R, int W, int GW>
-__global__ void __launch_bounds__((W + 1) * 32, 1) gemv_fast_kernel(const Params p) {
+__global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 2 : 1) gemv_fast_kernel(const Params p) {
     using F = Fmt<FMT>;
     constexpr int UE = F::UE;
     constexpr int NCH = UE / 4;       // float4 chunks of x per unit
@@ -760,8 +760,15 @@ int dispatch_gw(const DevCtx& dc, const Params& kp, int GW, int grid, int smem, 
 }
 
 template <int FMT>
-int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int grid, int smem,
-             bool pdl, cudaStream_t s) {
+int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int W, int grid,
+             int smem, bool pdl, cudaStream_t s) {
+    if (MT == 1 && W == 8) {
+        // Eight consumer warps and at most 113 registers: two CTAs (this launch's
+        // and the next one's) fit on an SM.
+        if (R <= 4) return dispatch_gw<FMT, 1, 8, 4>(dc, kp, GW, grid, smem, pdl, s);
+        if (R == 8) return dispatch_gw<FMT, 1, 8, 8>(dc, kp, GW, grid, smem, pdl, s);
+        return dispatch_gw<FMT, 1, 8, 16>(dc, kp, GW, grid, smem, pdl, s);
+    }
     switch (MT) {
         case 1:
             if (R <= 2) return dispatch_gw<FMT, 1, 16, 2>(dc, kp, GW, grid, smem, pdl, s);

@@ -3,9 +3,9 @@
 
 namespace qg {
 
-int fast_launch_aff_u8(const DevCtx& dc, const fast::Params& kp, int MT, int R, int GW, int grid,
+int fast_launch_aff_u8(const DevCtx& dc, const fast::Params& kp, int MT, int R, int GW, int W, int grid,
                    int smem, bool pdl, cudaStream_t s) {
-    return fast::dispatch<FMT_AFF_U8>(dc, kp, MT, R, GW, grid, smem, pdl, s);
+    return fast::dispatch<FMT_AFF_U8>(dc, kp, MT, R, GW, W, grid, smem, pdl, s);
 }
 
 }  // namespace qg

@@ -28,6 +28,7 @@ std::atomic<long long> g_opt_stream{1};
 std::atomic<long long> g_opt_stream_warps{0};
 std::atomic<long long> g_opt_stream_slots{0};
 std::atomic<long long> g_opt_ahead{2};
+std::atomic<long long> g_opt_staged_warps{0};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -150,6 +151,7 @@ long long launch_option(int option) {
         case QG_OPT_STREAM_WARPS: return g_opt_stream_warps.load(std::memory_order_relaxed);
         case QG_OPT_STREAM_SLOTS: return g_opt_stream_slots.load(std::memory_order_relaxed);
         case QG_OPT_STAGES_AHEAD: return g_opt_ahead.load(std::memory_order_relaxed);
+        case QG_OPT_STAGED_WARPS: return g_opt_staged_warps.load(std::memory_order_relaxed);
         default: return 0;
     }
 }
@@ -342,6 +344,10 @@ int qg_set_option(int option, int64_t value) {
             if (value < 0 || value > 64) return QG_ERR_INVALID_ARG;
             g_opt_ahead.store(value, std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_STAGED_WARPS:
+            if (value != 0 && value != 8) return QG_ERR_INVALID_ARG;
+            g_opt_staged_warps.store(value, std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }
@@ -361,6 +367,9 @@ int qg_get_option(int option, int64_t* value) {
             *value = g_opt_stream_slots.load(std::memory_order_relaxed);
             return QG_OK;
         case QG_OPT_STAGES_AHEAD: *value = g_opt_ahead.load(std::memory_order_relaxed); return QG_OK;
+        case QG_OPT_STAGED_WARPS:
+            *value = g_opt_staged_warps.load(std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }

@@ -212,8 +212,13 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * only once chunk i - n has landed, so that each SM's first chunks are not
  * queued behind the whole grid's traffic (tuning; a value above the ring size
  * means the ring size). */
+/*
+ * QG_OPT_STAGED_WARPS (default 0 = automatic; or 8): with 8, M = 1 calls of
+ * the staged-stage kernel use eight consumer warps and at most half an SM's
+ * registers and shared memory, so that the next launch's CTA can be resident
+ * beside this one (tuning). */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
-       QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6 };
+       QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6, QG_OPT_STAGED_WARPS = 7 };
 QG_API int qg_set_option(int option, int64_t value);
 QG_API int qg_get_option(int option, int64_t* value);
 

@@ -292,3 +292,19 @@ def test_stages_ahead_does_not_change_results(ahead):
         qg.set_option(qg.QG_OPT_STAGES_AHEAD, old)
     assert_bitwise(ya, base[0], f"ahead={ahead} y_a")
     assert_bitwise(yb, base[1], f"ahead={ahead} y_b")
+
+
+def test_eight_warp_coresident_variant_is_bitwise_equal():
+    """QG_OPT_STAGED_WARPS = 8 changes the CTA shape (and lets the next launch's
+    CTA share the SM), never an output's arithmetic."""
+    M, N, K = 1, 900, 4096
+    c = synth.q4_0_case(2400, N, K, M, dual=True)
+    wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
+    base = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    qg.set_option(qg.QG_OPT_STAGED_WARPS, 8)
+    try:
+        ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    finally:
+        qg.set_option(qg.QG_OPT_STAGED_WARPS, 0)
+    assert_bitwise(ya, base[0], "8-warp y_a")
+    assert_bitwise(yb, base[1], "8-warp y_b")
