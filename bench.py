@@ -302,6 +302,9 @@ def sweep_specs():
         ("cfg3 affine u8 M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 0)),
         ("cfg3 affine packed M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 1)),
         ("cfg4 qkv_split", lambda: make_qkv()),
+        # Q4_0 / Q4_K prefill: repacked to affine codes (group 32), tcgen05 MMAs.
+        ("prefill dual q4_0 N=K=4096 M=512", lambda: make_dual_q4_0(512, 4096, 4096, 80)),
+        ("prefill q4_k N=K=4096 M=512", lambda: make_single("q4_k", 512, 4096, 4096, 81)),
     ]
     for M in (1, 2, 4, 8):
         specs += [

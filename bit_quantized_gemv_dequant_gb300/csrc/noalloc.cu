@@ -51,7 +51,7 @@ int scratch_address(void** out) {
 extern "C" int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M, int64_t N,
                                   int64_t K, qg_stream_t stream) {
     size_t need = 0;
-    int rc = qg_workspace_size(QG_OP_Q4_K, M, N, K, 0, 0, &need);
+    int rc = qg::cuda_core_workspace_size(QG_OP_Q4_K, M, N, K, &need);
     if (rc != QG_OK) return rc;
     if (need > qg::kNoAllocScratchBytes) return QG_ERR_WORKSPACE;
     void* scratch = nullptr;

@@ -137,6 +137,10 @@ int run_gemv(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
         if (prefill_workspace_bytes(a) > (ws ? ws_bytes : 0)) return QG_ERR_WORKSPACE;
         return prefill_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
     }
+    // Q4_0 / Q4_K prefill on the tensor cores when the workspace holds the
+    // repacked weights; otherwise the CUDA-core path (smaller workspace).
+    if (quant_prefill_eligible(*dc, a) && ws && ws_bytes >= quant_prefill_workspace_bytes(a))
+        return quant_prefill_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
     if (gemv_workspace_bytes(*dc, a) > (ws ? ws_bytes : 0)) return QG_ERR_WORKSPACE;
     return gemv_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -159,6 +163,47 @@ long long launch_option(int option) {
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
     return QG_ERR_CUDA;
+}
+
+// Workspace bytes of op; with quant_prefill the Q4_0 / Q4_K tensor-core
+// prefill is included.
+int workspace_size_impl(int op, int64_t M, int64_t N, int64_t K, int group_size, int packed,
+                        size_t* bytes, bool quant_prefill) {
+    if (!bytes) return QG_ERR_INVALID_ARG;
+    *bytes = 0;
+    GemvArgs a{};
+    switch (op) {
+        case QG_OP_Q4_0: a.fmt = FMT_Q4_0; a.nw = 1; break;
+        case QG_OP_DUAL_Q4_0: a.fmt = FMT_Q4_0; a.nw = 2; break;
+        case QG_OP_Q4_K: a.fmt = FMT_Q4_K; a.nw = 1; break;
+        case QG_OP_AFFINE:
+            if (packed != 0 && packed != 1) return QG_ERR_INVALID_ARG;
+            a.fmt = packed ? FMT_AFF_PACKED : FMT_AFF_U8;
+            a.nw = 1;
+            a.gs = group_size;
+            break;
+        default: return QG_ERR_INVALID_ARG;
+    }
+    int rc = check_dims(M, N, K);
+    if (rc) return rc;
+    a.M = M; a.N = N; a.K = K;
+    // Plan with 16-byte aligned stand-in pointers: the size assumes the
+    // caller's buffers allow the fastest path (an upper bound otherwise).
+    static const uint8_t probe[16] __attribute__((aligned(16))) = {0};
+    a.w[0] = a.w[1] = probe;
+    a.scales = a.biases = a.x = reinterpret_cast<const float*>(probe);
+    const DevCtx* dc = nullptr;
+    rc = current_ctx(&dc);
+    if (rc) return rc;
+    *bytes = gemv_workspace_bytes(*dc, a);
+    if (prefill_eligible(*dc, a)) *bytes = std::max(*bytes, prefill_workspace_bytes(a));
+    if (quant_prefill && quant_prefill_eligible(*dc, a))
+        *bytes = std::max(*bytes, quant_prefill_workspace_bytes(a));
+    return QG_OK;
+}
+
+int cuda_core_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    return workspace_size_impl(op, M, N, K, 0, 0, bytes, false);
 }
 
 }  // namespace qg
@@ -287,36 +332,9 @@ int dequant_affine(const void* q, const float* scales, const float* biases, floa
 
 int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_size, int packed,
                       size_t* bytes) {
-    if (!bytes) return QG_ERR_INVALID_ARG;
-    *bytes = 0;
-    GemvArgs a{};
-    switch (op) {
-        case QG_OP_Q4_0: a.fmt = FMT_Q4_0; a.nw = 1; break;
-        case QG_OP_DUAL_Q4_0: a.fmt = FMT_Q4_0; a.nw = 2; break;
-        case QG_OP_Q4_K: a.fmt = FMT_Q4_K; a.nw = 1; break;
-        case QG_OP_AFFINE:
-            if (packed != 0 && packed != 1) return QG_ERR_INVALID_ARG;
-            a.fmt = packed ? FMT_AFF_PACKED : FMT_AFF_U8;
-            a.nw = 1;
-            a.gs = group_size;
-            break;
-        default: return QG_ERR_INVALID_ARG;
-    }
-    int rc = check_dims(M, N, K);
-    if (rc) return rc;
-    a.M = M; a.N = N; a.K = K;
-    // Plan with 16-byte aligned stand-in pointers: the size assumes the
-    // caller's buffers allow the fastest path (an upper bound otherwise).
-    static const uint8_t probe[16] __attribute__((aligned(16))) = {0};
-    a.w[0] = a.w[1] = probe;
-    a.scales = a.biases = a.x = reinterpret_cast<const float*>(probe);
-    const DevCtx* dc = nullptr;
-    rc = current_ctx(&dc);
-    if (rc) return rc;
-    *bytes = gemv_workspace_bytes(*dc, a);
-    if (prefill_eligible(*dc, a)) *bytes = std::max(*bytes, prefill_workspace_bytes(a));
-    return QG_OK;
+    return qg::workspace_size_impl(op, M, N, K, group_size, packed, bytes, true);
 }
+
 
 int qg_set_option(int option, int64_t value) {
     switch (option) {

@@ -142,6 +142,13 @@ bool prefill_eligible(const DevCtx& dc, const GemvArgs& a);
 size_t prefill_workspace_bytes(const GemvArgs& a);
 int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// Q4_0 / Q4_K prefill (prefill_repack.cu): the weights rewritten as packed
+// affine codes with group size 32 in the workspace, then the affine prefill.
+bool quant_prefill_eligible(const DevCtx& dc, const GemvArgs& a);
+size_t quant_prefill_workspace_bytes(const GemvArgs& a);
+int quant_prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes,
+                         cudaStream_t s);
+
 // Copies and dequantization (elementwise.cu).
 int qkv_split_launch(const DevCtx& dc, const float* qkv, float* q, float* k, float* v,
                      int64_t seq, int64_t q_sp, int64_t k_sp, int64_t v_sp, cudaStream_t s);
@@ -149,6 +156,10 @@ int dequant_launch(const DevCtx& dc, int fmt, const uint8_t* w, const float* sca
                    const float* biases, float* out, int64_t N, int64_t K, int gs,
                    cudaStream_t s);
 int selftest_wait_launch(const DevCtx& dc, long long timeout_ns, cudaStream_t s);
+
+// Workspace of the CUDA-core path alone (qg_workspace_size also covers the
+// Q4_0 / Q4_K tensor-core prefill, which calls with a smaller workspace skip).
+int cuda_core_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 // Record a CUDA error for qg_last_cuda_error() and return QG_ERR_CUDA.
 int cuda_fail(cudaError_t e);

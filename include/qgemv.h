@@ -92,7 +92,18 @@ enum {
 /* Single Q4_0 projection: y[M,N] = x[M,K] . dequant(w)[N,K]^T.
  * Page: fused_dual_proj_q4_0.rs (mlx-native 0.9.1) - the baseline
  * kernel_mul_mv_q4_0_f32 dispatch the fused op is defined against.
- * w: N*(K/32)*18 bytes; x: M*K f32; y: M*N f32. M, N, K > 0, K % 32 == 0. */
+ * w: N*(K/32)*18 bytes; x: M*K f32; y: M*N f32. M, N, K > 0, K % 32 == 0.
+ *
+ * Q4_0 and Q4_K calls take one of two paths:
+ * - CUDA cores, f32 (|y - exact| <= 1e-5 * sum_k |x w| + 1e-6), for every M.
+ * - Tensor cores (prefill), when M >= QG_OPT_PREFILL_MIN_M (default 16), x is
+ *   16-byte aligned, the tensor-core prefill conditions of qmm_affine hold for
+ *   group size 32, and the workspace is at least qg_workspace_size bytes. The
+ *   weights are rewritten in the workspace as packed affine codes per 32
+ *   weights (Q4_0: scale d, bias -8d; Q4_K: scale d*sc, bias -dmin*m, all
+ *   exact) and multiplied as qmm_affine's prefill does; the error bound is
+ *   qmm_affine's (2e-3 * sum_k |x w|). A smaller workspace (as small as the
+ *   CUDA-core path needs) keeps the call on CUDA cores. */
 QG_API int qgemv_q4_0(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
                void* workspace, size_t workspace_bytes, qg_stream_t stream);
 
@@ -108,7 +119,8 @@ QG_API int qgemv_dual_q4_0(const void* w_a, const void* w_b, const float* x, flo
                     qg_stream_t stream);
 
 /* Q4_K GEMV. Page: q4_k_gemv_v2.rs (ferrum-kernels 0.7.7),
- * dispatch_gemv_q4k_v2_offset (M = 1 there; any M here).
+ * dispatch_gemv_q4k_v2_offset (M = 1 there; any M here; the two paths of
+ * qgemv_q4_0 apply).
  * w: N*(K/256)*144 bytes; x: M*K f32; y: M*N f32. K % 256 == 0. Callers that
  * keep several tensors in one buffer pass offset pointers (byte offsets
  * must keep the stated alignment). */
@@ -129,7 +141,9 @@ QG_API int qgemv_q4_k(const void* w, const float* x, float* y, int64_t M, int64_
  *   capture.
  * - All calls share the one array: calls that may overlap on the GPU (other
  *   streams, other host threads) race on it. Its contents are fully rewritten
- *   before they are read, so nothing needs clearing between calls. */
+ *   before they are read, so nothing needs clearing between calls.
+ * - Always takes qgemv_q4_k's CUDA-core path: the tensor-core prefill needs a
+ *   workspace for the rewritten weights, which this entry point does not have. */
 QG_API int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M, int64_t N,
                               int64_t K, qg_stream_t stream);
 
