@@ -59,9 +59,11 @@ constexpr int kACol0 = kPBufs * kPCols;  // A buffers follow: 384 + 4 * 32 = 512
 constexpr int kXSlots = 32;    // ring of per-group activation sums in shared memory
 constexpr int kXSlotBytes = kTileT * 4;
 constexpr int kTmemCols = 512;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kEpiWarps = 8;  // epilogue warps 4 .. 4 + kEpiWarps - 1
+constexpr int kEpiCols = kTileT / (kEpiWarps / 4);  // activation rows (columns) per epilogue warp
+constexpr int kProducerWarp = 4 + kEpiWarps;
+constexpr int kMmaWarp = 5 + kEpiWarps;
+constexpr int kThreads = (6 + kEpiWarps) * 32;
 constexpr int kXhBytes = kTileT * kChunk * 2;  // 16 KB per stage
 constexpr int kPrepThreads = 256;
 
@@ -367,11 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kPBufs; ++i) {
             mbar_init(p_full(i), 1);
-            mbar_init(p_empty(i), 256);
+            mbar_init(p_empty(i), kEpiWarps * 32);
         }
         for (int i = 0; i < kXSlots; ++i) {
             mbar_init(x_full(i), 1);
-            mbar_init(x_empty(i), 256);
+            mbar_init(x_empty(i), kEpiWarps * 32);
         }
         mbar_init(done_bar, 1);
         fence_mbar_init();
@@ -543,17 +545,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++ab == kABufs) { ab = 0; aph ^= 1; }
             if (GK == 4 && ++gst == p.spgs) gst = 0;
         }
-    } else if (warp < 12) {
+    } else if (warp < 4 + kEpiWarps) {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;                 // tensor-memory lane quarter
-        const int half = (warp - 4) >> 2;       // which 64 activation rows
+        constexpr int kChunks = kEpiCols / 16;   // 16-column tensor-memory loads per group
+        const int q = warp & 3;                  // tensor-memory lane quarter
+        const int part = (warp - 4) >> 2;        // which kEpiCols activation rows
         const int n = n0 + q * 32 + lane;
         const bool nvalid = n < p.N;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const int t0 = m0 + half * 64;
-        float2 acc[32];
+        const int t0 = m0 + part * kEpiCols;
+        float2 acc[kEpiCols / 2];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.f, 0.f);
+        for (int c = 0; c < kEpiCols / 2; ++c) acc[c] = make_float2(0.f, 0.f);
         bool ok = true;
         // Column n of the transposed scales/biases: a warp's loads are coalesced.
         const float* srow = p.scales_t + (nvalid ? n : 0);
@@ -563,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Scale and bias of the next group are loaded one group ahead.
         float s_nx = nvalid ? __ldg(srow) : 0.f;
         float b_nx = nvalid ? __ldg(brow) : 0.f;
-        // acc[c] (tokens 2c, 2c+1 of this warp's 64) += s * P + b * X for one
-        // 16-column chunk hf of P.
+        // acc[c] (tokens 2c, 2c+1 of this warp's kEpiCols) += s * P + b * X for
+        // one 16-column chunk hf of P.
         auto fma_chunk = [&](int hf, const uint32_t (&r)[16], const float4 (&xv)[4], float2 s2,
                              float2 b2) {
 #pragma unroll
@@ -590,46 +593,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const float4* xs =
-                reinterpret_cast<const float4*>(smem + Gm::kXOff + xsl * kXSlotBytes) + half * 16;
-            const uint32_t pcol = tmem + lane_base + pb * kPCols + half * 64;
-            // Four 16-column chunks; the load of chunk hf+1 is in flight while
-            // chunk hf is multiplied.
+            const float4* xs = reinterpret_cast<const float4*>(smem + Gm::kXOff + xsl * kXSlotBytes) +
+                               part * (kEpiCols / 4);
+            const uint32_t pcol = tmem + lane_base + pb * kPCols + part * kEpiCols;
+            // 16-column chunks; the load of chunk hf+1 is in flight while chunk hf
+            // is multiplied.
             uint32_t ra[16], rb[16];
             float4 xv[4];
             tmem_ld16_async(pcol, ra);
             tmem_wait16(ra);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[c4];
-            tmem_ld16_async(pcol + 16, rb);
-            fma_chunk(0, ra, xv, s2, b2);
-            tmem_wait16(rb);
+            for (int hf = 0; hf < kChunks; ++hf) {
+                uint32_t(&cur)[16] = (hf & 1) ? rb : ra;
+                uint32_t(&nxt)[16] = (hf & 1) ? ra : rb;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[4 + c4];
-            tmem_ld16_async(pcol + 32, ra);
-            fma_chunk(1, rb, xv, s2, b2);
-            tmem_wait16(ra);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[8 + c4];
-            tmem_ld16_async(pcol + 48, rb);
-            fma_chunk(2, ra, xv, s2, b2);
-            tmem_wait16(rb);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[12 + c4];
-            // Everything of group j is read: release P and the sums.
-            tc_fence_before();
-            mbar_arrive(p_empty(pb));
-            mbar_arrive(x_empty(xsl));
-            fma_chunk(3, rb, xv, s2, b2);
+                for (int c4 = 0; c4 < 4; ++c4) xv[c4] = xs[4 * hf + c4];
+                if (hf + 1 < kChunks) tmem_ld16_async(pcol + 16 * (hf + 1), nxt);
+                if (hf + 1 == kChunks) {
+                    // Everything of group j is read: release P and the sums.
+                    tc_fence_before();
+                    mbar_arrive(p_empty(pb));
+                    mbar_arrive(x_empty(xsl));
+                }
+                fma_chunk(hf, cur, xv, s2, b2);
+                if (hf + 1 < kChunks) tmem_wait16(nxt);
+            }
             if (++pb == kPBufs) { pb = 0; pph ^= 1; }
             if (++xsl == kXSlots) { xsl = 0; xph ^= 1; }
         }
         if (ok) {
-            // Lane l holds 2^-e of activation rows t0 + 2l and t0 + 2l + 1.
-            const float2 iv = __ldg(reinterpret_cast<const float2*>(p.inv + t0) + lane);
+            // Lane l < kEpiCols / 2 holds 2^-e of activation rows t0 + 2l, t0 + 2l + 1.
+            const float2 iv = lane < kEpiCols / 2
+                                  ? __ldg(reinterpret_cast<const float2*>(p.inv + t0) + lane)
+                                  : make_float2(1.f, 1.f);
             float* yp = p.y + (size_t)t0 * p.N + (nvalid ? n : 0);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < kEpiCols / 2; ++c) {
                 const float2 sc = make_float2(__shfl_sync(0xFFFFFFFFu, iv.x, c),
                                               __shfl_sync(0xFFFFFFFFu, iv.y, c));
                 const int m = t0 + 2 * c;
