@@ -216,14 +216,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ------------------------------------------------------------- prep kernel
-// Blocks [0, Mp) prepare activation rows; blocks [Mp, Mp + tiles) transpose
-// 32 x 32 tiles of the scales and biases to [G, N], so that the main
-// kernel's epilogue (one weight row per thread) reads them coalesced.
+// Blocks [0, Mp) prepare activation rows (with xsum = nullptr, no group
+// sums). The blocks after them transpose 32 x 32 tiles of the scales and
+// biases to [G, N], so that a kernel handling one weight row per thread reads
+// them coalesced; with bpart given they also write, per weight row and tile,
+// the bound max_g (|s| * qmax + |b|) over the tile's 32 groups
+// (bpart[n * ceil(G / 32) + tile]) for fold_kernel.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
     const float* __restrict__ x, __half* __restrict__ xh, float* __restrict__ xsum,
     float* __restrict__ inv, const float* __restrict__ sc, const float* __restrict__ bi,
-    float* __restrict__ sc_t, float* __restrict__ bi_t, int M, int N, int K, int gs, int G,
-    int Mp) {
+    float* __restrict__ sc_t, float* __restrict__ bi_t, float* __restrict__ bpart, float qmax,
+    int M, int N, int K, int gs, int G, int Mp) {
     __shared__ float red[kPrepThreads / 32];
     __shared__ float amax_s;
     __shared__ float tile[2][32][33];
@@ -236,8 +239,16 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
         for (int r = ty; r < 32; r += 8) {
             const int n = n_0 + r, g = g_0 + tx;
             const bool in = n < N && g < G;
-            tile[0][r][tx] = in ? __ldg(sc + (size_t)n * G + g) : 0.f;
-            tile[1][r][tx] = in ? __ldg(bi + (size_t)n * G + g) : 0.f;
+            const float sv = in ? __ldg(sc + (size_t)n * G + g) : 0.f;
+            const float bv = in ? __ldg(bi + (size_t)n * G + g) : 0.f;
+            tile[0][r][tx] = sv;
+            tile[1][r][tx] = bv;
+            if (bpart) {
+                float mx = fmaf(fabsf(sv), qmax, fabsf(bv));
+#pragma unroll
+                for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                if (tx == 0 && n < N) bpart[(size_t)n * tiles_g + g_0 / 32] = mx;
+            }
         }
         __syncthreads();
         for (int r = ty; r < 32; r += 8) {
@@ -252,7 +263,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
     const int m = blockIdx.x;
     const int lane = t & 31, warp = t >> 5;
     if (m >= M) {  // padding rows: zero group sums so the epilogue reads defined values
-        for (int g = t; g < G; g += kPrepThreads) xsum[(size_t)g * Mp + m] = 0.f;
+        if (xsum)
+            for (int g = t; g < G; g += kPrepThreads) xsum[(size_t)g * Mp + m] = 0.f;
         if (t == 0) inv[m] = 1.f;
         return;
     }
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
         }
         for (int o = width >> 1; o; o >>= 1) f += __shfl_xor_sync(0xFFFFFFFFu, f, o);
         if ((gs >> 2) <= 32) {
-            if ((lane & (width - 1)) == 0 && c < quads) {
+            if (xsum && (lane & (width - 1)) == 0 && c < quads) {
                 const int g = (c << 2) >> (__ffs(gs) - 1);
                 xsum[(size_t)g * Mp + m] = f;
             }
@@ -315,7 +327,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
                 float s = 0.f;
                 for (int w = 0; w < wpg; ++w) s += red[t * wpg + w];
                 const int g = base / (gs >> 2) + t;
-                if (g < G) xsum[(size_t)g * Mp + m] = s;
+                if (xsum && g < G) xsum[(size_t)g * Mp + m] = s;
             }
             __syncthreads();
         }
@@ -651,6 +663,307 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// --------------------------------------------------- folded-weight kernel
+// The default prefill kernel. Scale and bias are folded into the weights
+// before the tensor cores see them, so a single accumulator in tensor memory
+// spans all of K and the epilogue runs once per tile:
+//
+//     w'[n,k] = fp16_rn( (s[n,g] * q[n,k] + b[n,g]) * 2^f_n ),
+//     y[m,n]  = ( sum_k w'[n,k] * xh[m,k] ) * 2^-f_n * 2^-e_m.
+//
+// f_n puts the row's bound max_g (|s| * qmax + |b|) in [2^14, 2^15), so no
+// w' overflows fp16 and every weight above 2^-29 of that bound keeps a
+// relative rounding error of at most 2^-11, as xh does. The product error is
+// then at most about 2^-10 * sum_k |x w| plus the f32 accumulation: within
+// the 2e-3 * sum_k |x w| prefill tolerance. The value s * q + b is formed in
+// f32 from the exact code q (2^23 + q through a byte permute, minus 2^23),
+// so cancellation between s * q and b costs nothing before the one rounding
+// to fp16.
+//
+//   warps 0-15  converters, then epilogue. Warp w handles weight rows
+//               32 * (w % 4) .. + 31 (its tensor-memory lane quarter), the
+//               k half (w / 4) % 2 of the 64-wide stages of parity w / 8:
+//               codes -> w' in registers -> tcgen05.st into the A buffer.
+//               Two warps per lane quarter and stage, and two stages in
+//               conversion at once, hide the latency of each stage's chain
+//               (barrier wait, shared-memory loads, conversion, tensor-memory
+//               store and its wait).
+//   warp 16     TMA producer (codes and xh tiles, as in mma_kernel).
+//   warp 17     MMA issuer: four K = 16 MMAs per stage into one accumulator.
+constexpr int kFStages = 8;
+constexpr int kFABufs = 8;              // A buffers, 32 columns each
+constexpr int kFAcc = 0;                // accumulator columns [0, kTileT)
+constexpr int kFACol0 = kTileT;         // A buffers: columns [128, 384)
+constexpr int kFConv = 16;              // converter / epilogue warps
+constexpr int kFStageWarps = 8;         // converter warps per stage
+constexpr int kFProducer = kFConv;
+constexpr int kFMma = kFConv + 1;
+constexpr int kFThreads = (kFConv + 2) * 32;
+static_assert(kFACol0 + kFABufs * 32 <= kTmemCols, "tensor memory columns");
+static_assert(kFStages % 2 == 0 && kFABufs % 2 == 0, "stage parities own disjoint buffers");
+
+template <bool PACKED>
+struct GeoF {
+    static constexpr int kStageBytes = Geo<PACKED>::kStageBytes;
+    static constexpr int kBarOff = kFStages * kStageBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOff + 1024;
+};
+
+struct FoldParams {
+    const float* scales_t;  // [G, N]
+    const float* biases_t;  // [G, N]
+    const float* bpart;     // [N, GT] max_g (|s| * qmax + |b|) over 32-group tiles
+    const float* inv;       // [Mp] 2^-e_m
+    float* y;               // [M, N]
+    int M, N, K, G, GT;
+    int log2gs;
+    unsigned* err;
+};
+
+// Four codes (bytes of v) -> 2^23 + q as f32 bit patterns, two pairs.
+__device__ __forceinline__ void bytes_to_magic(uint32_t v, float2& q01, float2& q23) {
+    q01 = make_float2(__uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u)),
+                      __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7441u)));
+    q23 = make_float2(__uint_as_float(__byte_perm(v, 0x4B000000u, 0x7442u)),
+                      __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7443u)));
+}
+
+// (2^23 + q) pair -> fp16x2 of s * q + b (low half: the first element).
+__device__ __forceinline__ uint32_t fold_pair(float2 magic, float2 s2, float2 b2) {
+    const float2 q = __fadd2_rn(magic, make_float2(-8388608.f, -8388608.f));  // exact
+    const float2 w = __ffma2_rn(s2, q, b2);
+    const __half2 hw = __floats2half2_rn(w.x, w.y);
+    return *reinterpret_cast<const uint32_t*>(&hw);
+}
+
+template <bool PACKED, bool GS16>
+__global__ void __launch_bounds__(kFThreads, 1)
+    fold_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_x,
+                const FoldParams p) {
+    using Gm = GeoF<PACKED>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t bars = base + Gm::kBarOff;
+    auto full = [&](int i) { return bars + 8u * i; };
+    auto empty = [&](int i) { return bars + 8u * (kFStages + i); };
+    auto a_full = [&](int i) { return bars + 8u * (2 * kFStages + i); };
+    auto a_empty = [&](int i) { return bars + 8u * (2 * kFStages + kFABufs + i); };
+    constexpr int kDone = 2 * kFStages + 2 * kFABufs;
+    const uint32_t done_bar = bars + 8u * kDone;
+    static_assert(8 * (kDone + 1) + 4 <= 1024, "barrier area");
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + 8 * (kDone + 1));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kTileT;
+    const int n0 = blockIdx.y * kTileN;
+    const int nstages = (p.K + kChunk - 1) / kChunk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kFStages; ++i) {
+            mbar_init(full(i), 1);
+            mbar_init(empty(i), 1);
+        }
+        for (int i = 0; i < kFABufs; ++i) {
+            mbar_init(a_full(i), kFStageWarps * 32);
+            mbar_init(a_empty(i), 1);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == kFMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kFProducer) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&map_q);
+            prefetch_tmap(&map_x);
+            int issued = 0;
+            for (int i = 0; i < nstages; ++i) {
+                const int st = i % kFStages;
+                if (i >= kFStages && !mbar_wait(empty(st), ((i / kFStages) & 1) ^ 1)) {
+                    report_error(p.err, DEVERR_TC_WAIT);
+                    break;
+                }
+                const uint32_t sb = base + st * Gm::kStageBytes;
+                mbar_arrive_expect_tx(full(st), Gm::kStageBytes);
+                tma_load_2d(sb, &map_x, i * kChunk, m0, full(st));
+                tma_load_2d(sb + kXhBytes, &map_q, i * Geo<PACKED>::kCodeRowBytes, n0, full(st));
+                issued = i + 1;
+            }
+            // Copies must land before the CTA can exit, whatever happened above.
+            for (int i = max(0, issued - kFStages); i < issued; ++i)
+                if (!mbar_wait(full(i % kFStages), (i / kFStages) & 1))
+                    report_error(p.err, DEVERR_WAIT_DRAIN);
+        }
+    } else if (warp == kFMma) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int st = 0, ab = 0;
+            uint32_t aph = 0;
+            for (int i = 0; i < nstages; ++i) {
+                // a_full implies the stage's copies landed: the converters waited for them.
+                if (!mbar_wait(a_full(ab), aph)) {
+                    report_error(p.err, DEVERR_TC_WAIT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sb = base + st * Gm::kStageBytes;
+                const uint32_t aa = tmem + kFACol0 + ab * 32;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_ts(tmem + kFAcc, aa + kk * 8, sw128_desc(sb + kk * 32), kIdesc,
+                              (i | kk) ? 1u : 0u);
+                tc_commit(empty(st));
+                tc_commit(a_empty(ab));
+                if (++st == kFStages) st = 0;
+                if (++ab == kFABufs) { ab = 0; aph ^= 1; }
+            }
+            tc_commit(done_bar);
+            if (!mbar_wait(done_bar, 0)) report_error(p.err, DEVERR_WAIT_DRAIN);
+        }
+    } else {
+        // ------------------------------------------------ converters, epilogue
+        const int qd = warp & 3;                   // tensor-memory lane quarter
+        const int h = (warp >> 2) & 1;             // k half of each stage
+        const int par = warp >> 3;                 // stages of this parity
+        const int row = qd * 32 + lane;
+        const int n = n0 + row;
+        const bool nvalid = n < p.N;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        int f = 0;
+        {
+            float bm = 0.f;
+            if (nvalid)
+                for (int j = 0; j < p.GT; ++j) bm = fmaxf(bm, __ldg(p.bpart + (size_t)n * p.GT + j));
+            if (bm > 0.f && bm <= 3.402823466e38f) {
+                int ex;
+                frexpf(bm, &ex);  // bm < 2^ex
+                f = min(120, max(-120, 15 - ex));
+            }
+        }
+        const float pw = __int_as_float((127 + f) << 23);
+        const float ipw = __int_as_float((127 - f) << 23);
+        // Raw scale and bias of the groups of stage i's k half: the first and
+        // the second 16 k (the same group unless gs = 16). Column n of the
+        // transposed [G, N] arrays: a warp's loads are coalesced.
+        auto load_sb = [&](int i, float (&sb4)[4]) {
+            const int k0 = i * kChunk + h * 32;
+            const int ga = k0 >> p.log2gs;
+            const int gb = GS16 ? ga + 1 : ga;
+            const bool va = nvalid && ga < p.G, vb = nvalid && gb < p.G;
+            sb4[0] = va ? __ldg(p.scales_t + (size_t)ga * p.N + n) : 0.f;
+            sb4[1] = va ? __ldg(p.biases_t + (size_t)ga * p.N + n) : 0.f;
+            sb4[2] = GS16 ? (vb ? __ldg(p.scales_t + (size_t)gb * p.N + n) : 0.f) : sb4[0];
+            sb4[3] = GS16 ? (vb ? __ldg(p.biases_t + (size_t)gb * p.N + n) : 0.f) : sb4[1];
+        };
+        float nx[4];
+        load_sb(par, nx);
+        bool ok = true;
+        for (int i = par; i < nstages; i += 2) {
+            const int st = i % kFStages, ab = i % kFABufs;
+            const uint32_t fph = (uint32_t)(i / kFStages) & 1u, aph = (uint32_t)(i / kFABufs) & 1u;
+            // Scaled by 2^f only here, one stage after the loads were issued.
+            const float2 sA = make_float2(nx[0] * pw, nx[0] * pw), bA = make_float2(nx[1] * pw, nx[1] * pw);
+            const float2 sB = make_float2(nx[2] * pw, nx[2] * pw), bB = make_float2(nx[3] * pw, nx[3] * pw);
+            if (i + 2 < nstages) load_sb(i + 2, nx);
+            if (!warp_wait(full(st), fph) || (i >= kFABufs && !warp_wait(a_empty(ab), aph ^ 1))) {
+                if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint8_t* cb = smem + st * Gm::kStageBytes + kXhBytes;
+            uint32_t o[16];
+            if (!PACKED) {
+                // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * h + cc;
+                    const uint4 v = *reinterpret_cast<const uint4*>(
+                        cb + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                    const float2 s2 = cc ? sB : sA, b2 = cc ? bB : bA;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float2 q01, q23;
+                        bytes_to_magic(w4[e], q01, q23);
+                        o[8 * cc + 2 * e] = fold_pair(q01, s2, b2);
+                        o[8 * cc + 2 * e + 1] = fold_pair(q23, s2, b2);
+                    }
+                }
+            } else {
+                // 32-byte swizzle: chunk c of row r sits at chunk c ^ ((r >> 2) & 1).
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    cb + row * 32 + ((h ^ ((row >> 2) & 1)) << 4));
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    // byte i: low nibble = k 8e + 2i, high nibble = k 8e + 2i + 1
+                    const uint32_t lo = w4[e] & 0x0F0F0F0Fu;
+                    const uint32_t hi = (w4[e] >> 4) & 0x0F0F0F0Fu;
+                    const float2 s2 = e < 2 ? sA : sB, b2 = e < 2 ? bA : bB;
+                    float2 l01, l23, h01, h23;
+                    bytes_to_magic(lo, l01, l23);
+                    bytes_to_magic(hi, h01, h23);
+                    o[4 * e + 0] = fold_pair(make_float2(l01.x, h01.x), s2, b2);
+                    o[4 * e + 1] = fold_pair(make_float2(l01.y, h01.y), s2, b2);
+                    o[4 * e + 2] = fold_pair(make_float2(l23.x, h23.x), s2, b2);
+                    o[4 * e + 3] = fold_pair(make_float2(l23.y, h23.y), s2, b2);
+                }
+            }
+            tmem_st16(tmem + lane_base + kFACol0 + ab * 32 + h * 16, o);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(a_full(ab));
+        }
+        // Epilogue: this warp's 32 activation rows (columns (w / 4) * 32 ..) of its lanes.
+        if (ok && warp_wait(done_bar, 0)) {
+            tc_fence_after();
+            const int c0 = (warp >> 2) * 32;
+            // Lane l holds 2^-e of activation row m0 + c0 + l.
+            const float ivl = __ldg(p.inv + m0 + c0 + lane);
+            float* yp = p.y + (size_t)(m0 + c0) * p.N + (nvalid ? n : 0);
+#pragma unroll
+            for (int cb16 = 0; cb16 < 2; ++cb16) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lane_base + kFAcc + c0 + cb16 * 16, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = cb16 * 16 + j;
+                    const float ivm = __shfl_sync(0xFFFFFFFFu, ivl, col);
+                    if (nvalid && m0 + c0 + col < p.M)
+                        yp[(size_t)col * p.N] = (__uint_as_float(r[j]) * ipw) * ivm;
+                }
+            }
+        } else if (ok) {
+            if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kFMma) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------------- host
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -672,7 +985,7 @@ int encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
 }
 
 struct Layout {
-    size_t xh, xsum, inv, sc_t, bi_t, total;
+    size_t xh, xsum, inv, sc_t, bi_t, bpart, total;
     int Mp, G;
 };
 
@@ -686,7 +999,8 @@ Layout layout(const GemvArgs& a) {
     L.inv = L.xsum + up((size_t)L.G * L.Mp * 4);
     L.sc_t = L.inv + up((size_t)L.Mp * 4);
     L.bi_t = L.sc_t + up((size_t)L.G * a.N * 4);
-    L.total = L.bi_t + up((size_t)L.G * a.N * 4);
+    L.bpart = L.bi_t + up((size_t)L.G * a.N * 4);
+    L.total = L.bpart + up((size_t)a.N * ((L.G + 31) / 32) * 4);
     return L;
 }
 
@@ -706,6 +1020,22 @@ int launch_main(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx, 
     return e == cudaSuccess ? QG_OK : cuda_fail(e);
 }
 
+template <bool PACKED, bool GS16>
+int launch_fold(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx,
+                const FoldParams& kp, dim3 grid, cudaStream_t s) {
+    constexpr int smem = GeoF<PACKED>::kSmemBytes;
+    static int configured[64] = {0};
+    auto kern = fold_kernel<PACKED, GS16>;
+    if (dc.device >= 0 && dc.device < 64 && !configured[dc.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured[dc.device] = 1;
+    }
+    kern<<<grid, kFThreads, smem, s>>>(mq, mx, kp);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
 }  // namespace prefill
 
 bool prefill_eligible(const DevCtx& dc, const GemvArgs& a) {
@@ -718,7 +1048,8 @@ bool prefill_eligible(const DevCtx& dc, const GemvArgs& a) {
     if (a.N > 65535ll * prefill::kTileN) return false;
     if ((reinterpret_cast<uintptr_t>(a.w[0]) & 15) || (reinterpret_cast<uintptr_t>(a.x) & 15))
         return false;
-    if (dc.max_smem_optin < prefill::Geo<false>::kSmemBytes) return false;
+    if (dc.max_smem_optin < std::max(prefill::Geo<false>::kSmemBytes, prefill::GeoF<false>::kSmemBytes))
+        return false;
     return true;
 }
 
@@ -763,11 +1094,38 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
 
     float* sc_t = reinterpret_cast<float*>(w8 + L.sc_t);
     float* bi_t = reinterpret_cast<float*>(w8 + L.bi_t);
+    float* bpart = reinterpret_cast<float*>(w8 + L.bpart);
+    const dim3 grid(L.Mp / kTileT, (unsigned)((a.N + kTileN - 1) / kTileN));
     const long long tiles = ((a.N + 31) / 32) * (long long)((L.G + 31) / 32);
     if (tiles > 0x7FFFFFFFll - L.Mp) return QG_ERR_UNSUPPORTED;
+    if (!launch_option(QG_OPT_PREFILL_EXACT)) {
+        prep_kernel<<<(unsigned)(L.Mp + tiles), kPrepThreads, 0, s>>>(
+            a.x, xh, nullptr, inv, a.scales, a.biases, sc_t, bi_t, bpart,
+            packed ? 15.f : 255.f, (int)a.M, (int)a.N, (int)a.K, a.gs, L.G, L.Mp);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+        FoldParams fp{};
+        fp.scales_t = sc_t;
+        fp.biases_t = bi_t;
+        fp.bpart = bpart;
+        fp.GT = (L.G + 31) / 32;
+        fp.inv = inv;
+        fp.y = a.y[0];
+        fp.M = (int)a.M;
+        fp.N = (int)a.N;
+        fp.K = (int)a.K;
+        fp.G = L.G;
+        fp.log2gs = __builtin_ctz((unsigned)a.gs);
+        fp.err = dc.err;
+        if (a.gs == 16)
+            return packed ? launch_fold<true, true>(dc, mq, mx, fp, grid, s)
+                          : launch_fold<false, true>(dc, mq, mx, fp, grid, s);
+        return packed ? launch_fold<true, false>(dc, mq, mx, fp, grid, s)
+                      : launch_fold<false, false>(dc, mq, mx, fp, grid, s);
+    }
     prep_kernel<<<(unsigned)(L.Mp + tiles), kPrepThreads, 0, s>>>(
-        a.x, xh, xsum, inv, a.scales, a.biases, sc_t, bi_t, (int)a.M, (int)a.N, (int)a.K, a.gs,
-        L.G, L.Mp);
+        a.x, xh, xsum, inv, a.scales, a.biases, sc_t, bi_t, nullptr, 0.f, (int)a.M, (int)a.N,
+        (int)a.K, a.gs, L.G, L.Mp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
 
@@ -785,7 +1143,6 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
     kp.gs = a.gs;
     kp.spgs = a.gs >= kChunk ? a.gs / kChunk : 1;
     kp.err = dc.err;
-    const dim3 grid(L.Mp / kTileT, (unsigned)((a.N + kTileN - 1) / kTileN));
     if (a.gs == 16)
         return packed ? launch_main<true, 1>(dc, mq, mx, kp, grid, s)
                       : launch_main<false, 1>(dc, mq, mx, kp, grid, s);

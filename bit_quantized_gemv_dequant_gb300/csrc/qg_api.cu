@@ -29,6 +29,7 @@ std::atomic<long long> g_opt_stream_warps{0};
 std::atomic<long long> g_opt_stream_slots{0};
 std::atomic<long long> g_opt_ahead{2};
 std::atomic<long long> g_opt_staged_warps{0};
+std::atomic<long long> g_opt_prefill_exact{0};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -156,6 +157,7 @@ long long launch_option(int option) {
         case QG_OPT_STREAM_SLOTS: return g_opt_stream_slots.load(std::memory_order_relaxed);
         case QG_OPT_STAGES_AHEAD: return g_opt_ahead.load(std::memory_order_relaxed);
         case QG_OPT_STAGED_WARPS: return g_opt_staged_warps.load(std::memory_order_relaxed);
+        case QG_OPT_PREFILL_EXACT: return g_opt_prefill_exact.load(std::memory_order_relaxed);
         default: return 0;
     }
 }
@@ -366,6 +368,10 @@ int qg_set_option(int option, int64_t value) {
             if (value != 0 && value != 8) return QG_ERR_INVALID_ARG;
             g_opt_staged_warps.store(value, std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_PREFILL_EXACT:
+            if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
+            g_opt_prefill_exact.store(value, std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }
@@ -387,6 +393,9 @@ int qg_get_option(int option, int64_t* value) {
         case QG_OPT_STAGES_AHEAD: *value = g_opt_ahead.load(std::memory_order_relaxed); return QG_OK;
         case QG_OPT_STAGED_WARPS:
             *value = g_opt_staged_warps.load(std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_PREFILL_EXACT:
+            *value = g_opt_prefill_exact.load(std::memory_order_relaxed);
             return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }

@@ -6,7 +6,10 @@ with ref and the sum from the oracle in f64. A second, tighter check pins the
 path's one approximation: rounding each activation row, scaled by a power of
 two, to fp16. Feeding those rounded activations to the oracle must reproduce
 y within the f32 bar (1e-5), so no other error source (a wrong group, scale,
-bias or tile) can hide inside the looser tolerance.
+bias or tile) can hide inside the looser tolerance. The folded-weight kernel
+(the default) also rounds each weight row, scaled by a power of two, to fp16;
+its tighter check feeds the oracle both rounded operands. Every tensor-core
+test runs on both kernels (QG_OPT_PREFILL_EXACT 0 and 1).
 
 Shapes span several 128x128 tiles with ragged tails in M, N and K, every
 group size the path takes (16 .. 1024), both code storages, 8-bit codes, and
@@ -36,6 +39,14 @@ def min_m():
     qg.set_option(qg.QG_OPT_PREFILL_MIN_M, old)
 
 
+@pytest.fixture(params=[0, 1], ids=["fold", "exact"])
+def kernel(request):
+    old = qg.get_option(qg.QG_OPT_PREFILL_EXACT)
+    qg.set_option(qg.QG_OPT_PREFILL_EXACT, request.param)
+    yield request.param
+    qg.set_option(qg.QG_OPT_PREFILL_EXACT, old)
+
+
 def _run(c, gs, packed, M=None):
     q = c["q_packed"] if packed else c["q"]
     return qg.qmm_affine(to_dev(c["x"]), to_dev(q), to_dev(c["s"]), to_dev(c["b"]), gs, packed)
@@ -58,6 +69,42 @@ def _rounded_x(x):
     return out
 
 
+def _rounded_w(W, rowbound):
+    """The folded kernel's weights: row n scaled by 2^f (f puts the row's bound
+    max_g (|s| qmax + |b|) into [2^14, 2^15)), rounded to fp16, scaled back."""
+    W = np.asarray(W, dtype=np.float64)
+    out = np.empty(W.shape, dtype=np.float32)
+    for n in range(W.shape[0]):
+        bm = np.float32(rowbound[n])
+        f = 0
+        if 0.0 < bm < np.inf:
+            _, ex = np.frexp(bm)
+            f = int(min(120, max(-120, 15 - int(ex))))
+        h = np.ldexp(W[n], f).astype(np.float16).astype(np.float64)
+        out[n] = np.ldexp(h, -f).astype(np.float32)
+    return out
+
+
+def affine_rowbound(s, b, qmax):
+    return np.max(np.abs(np.asarray(s, np.float32)) * np.float32(qmax)
+                  + np.abs(np.asarray(b, np.float32)), axis=1)
+
+
+def rounded_ref(x, W, rowbound, M, N, K):
+    """Oracle (f64) on the operands the folded kernel multiplies."""
+    return oracle.gemv_dense(_rounded_w(W, rowbound), _rounded_x(x), M, N, K)
+
+
+def check_rounding_only(y, kernel, x, q, s, b, M, N, K, gs, qmax, what):
+    """The f32 bar against the oracle fed the kernel's rounded operands."""
+    if kernel:
+        ref, bound = oracle.qmm_affine(_rounded_x(x), q, s, b, M, N, K, gs, False)
+    else:
+        W = oracle.dequant_affine(q, s, b, N, K, gs, False)
+        ref, bound = rounded_ref(x, W, affine_rowbound(s, b, qmax), M, N, K)
+    assert_parity(y, ref, bound, what=what)
+
+
 SHAPES = [
     # M,   N,   K,    gs
     (16, 128, 256, 64),
@@ -72,7 +119,7 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("M,N,K,gs", SHAPES)
-def test_prefill_parity_and_packed_equals_u8(M, N, K, gs):
+def test_prefill_parity_and_packed_equals_u8(M, N, K, gs, kernel):
     c = synth.affine_case(4100 + M + N + gs, N, K, M, gs)
     yu = _run(c, gs, 0)
     yp = _run(c, gs, 1)
@@ -82,26 +129,28 @@ def test_prefill_parity_and_packed_equals_u8(M, N, K, gs):
 
 
 @pytest.mark.parametrize("M,N,K,gs", SHAPES[:4])
-def test_prefill_error_is_only_fp16_rounding_of_x(M, N, K, gs):
+def test_prefill_error_is_only_fp16_rounding(M, N, K, gs, kernel):
     c = synth.affine_case(4200 + M + gs, N, K, M, gs)
     y = _run(c, gs, 0)
-    xr = _rounded_x(c["x"])
-    ref, bound = oracle.qmm_affine(xr, c["q"], c["s"], c["b"], M, N, K, gs, False)
-    assert_parity(y, ref, bound, what=f"prefill vs rounded-x oracle M={M} gs={gs}")
+    check_rounding_only(y, kernel, c["x"], c["q"], c["s"], c["b"], M, N, K, gs, 255,
+                        f"prefill vs rounded-operand oracle M={M} gs={gs}")
+    yp = _run(c, gs, 1)
+    check_rounding_only(yp, kernel, c["x"], c["q"], c["s"], c["b"], M, N, K, gs, 15,
+                        f"packed prefill vs rounded-operand oracle M={M} gs={gs}")
 
 
-def test_prefill_8bit_codes():
+def test_prefill_8bit_codes(kernel):
     M, N, K, gs = 200, 300, 1024, 64
     c = synth.affine_case(4300, N, K, M, gs)
     q8 = synth.codes(4301, (N, K), bits=8)
     y = qg.qmm_affine(to_dev(c["x"]), to_dev(q8), to_dev(c["s"]), to_dev(c["b"]), gs, 0)
     ref, bound = oracle.qmm_affine(c["x"], q8, c["s"], c["b"], M, N, K, gs, False)
     assert_parity(y, ref, bound, rel=REL_TC, what="prefill 8-bit codes")
-    ref_r, bound_r = oracle.qmm_affine(_rounded_x(c["x"]), q8, c["s"], c["b"], M, N, K, gs, False)
-    assert_parity(y, ref_r, bound_r, what="prefill 8-bit codes vs rounded-x oracle")
+    check_rounding_only(y, kernel, c["x"], q8, c["s"], c["b"], M, N, K, gs, 255,
+                        "prefill 8-bit codes vs rounded-operand oracle")
 
 
-def test_prefill_row_scaling_extremes():
+def test_prefill_row_scaling_extremes(kernel):
     """Rows far outside fp16's range (1e6, 1e-20) and an all-zero row: the
     per-row power-of-two scale keeps them exact up to fp16 rounding."""
     M, N, K, gs = 32, 160, 512, 64
@@ -117,8 +166,33 @@ def test_prefill_row_scaling_extremes():
     assert np.all(y.cpu().numpy()[2] == 0.0)
 
 
+def test_prefill_weight_row_extremes(kernel):
+    """Weight rows far outside fp16's range (scales and biases times 1e6 and
+    1e-20), an all-zero row, and a row whose groups differ by 2^10 in scale:
+    the folded kernel's per-row power of two keeps them within the bar."""
+    M, N, K, gs = 40, 140, 512, 64
+    c = synth.affine_case(4450, N, K, M, gs)
+    s, b = c["s"].copy(), c["b"].copy()
+    s[0] *= np.float32(1e6)
+    b[0] *= np.float32(1e6)
+    s[1] *= np.float32(1e-20)
+    b[1] *= np.float32(1e-20)
+    s[2] = 0.0
+    b[2] = 0.0
+    s[3, 1] *= np.float32(1024.0)
+    b[3, 1] *= np.float32(1024.0)
+    for packed in (0, 1):
+        q = c["q_packed"] if packed else c["q"]
+        y = qg.qmm_affine(to_dev(c["x"]), to_dev(q), to_dev(s), to_dev(b), gs, packed)
+        ref, bound = oracle.qmm_affine(c["x"], c["q"], s, b, M, N, K, gs, False)
+        assert_parity(y, ref, bound, rel=REL_TC, what=f"prefill extreme weight rows packed={packed}")
+        check_rounding_only(y, kernel, c["x"], c["q"], s, b, M, N, K, gs, 15 if packed else 255,
+                            f"extreme weight rows vs rounded-operand oracle packed={packed}")
+        assert np.all(y.cpu().numpy()[:, 2] == 0.0)
+
+
 @pytest.mark.parametrize("packed", [0, 1])
-def test_prefill_full_workload_sampled(packed):
+def test_prefill_full_workload_sampled(packed, kernel):
     """512 x 4096 x 4096, gs 64: the benchmarked launch. The oracle computes
     every activation row for 96 sampled weight rows, spread over all 32
     weight tiles (first and last row of each included)."""
@@ -137,7 +211,7 @@ def test_prefill_full_workload_sampled(packed):
     assert_parity(yh[:, rows], ref[:, rows], bound[:, rows], rel=REL_TC, what="full workload")
 
 
-def test_prefill_min_m_option_selects_path(min_m):
+def test_prefill_min_m_option_selects_path(min_m, kernel):
     M, N, K, gs = 24, 96, 512, 64
     c = synth.affine_case(4500, N, K, M, gs)
     ref, bound = oracle.qmm_affine(c["x"], c["q"], c["s"], c["b"], M, N, K, gs, False)
@@ -147,9 +221,8 @@ def test_prefill_min_m_option_selects_path(min_m):
     qg.set_option(qg.QG_OPT_PREFILL_MIN_M, 1)        # tensor cores, even M=1
     y_tc = _run(c, gs, 0)
     assert_parity(y_tc, ref, bound, rel=REL_TC, what="tensor-core path M=24")
-    xr = _rounded_x(c["x"])
-    ref_r, bound_r = oracle.qmm_affine(xr, c["q"], c["s"], c["b"], M, N, K, gs, False)
-    assert_parity(y_tc, ref_r, bound_r, what="tensor-core path M=24 vs rounded x")
+    check_rounding_only(y_tc, kernel, c["x"], c["q"], c["s"], c["b"], M, N, K, gs, 255,
+                        "tensor-core path M=24 vs rounded operands")
     c1 = synth.affine_case(4501, N, K, 1, gs)
     y1 = _run(c1, gs, 1)
     ref1, bound1 = oracle.qmm_affine(c1["x"], c1["q"], c1["s"], c1["b"], 1, N, K, gs, False)
@@ -173,7 +246,7 @@ def test_prefill_small_group_size_falls_back_to_cuda_cores():
     assert_parity(y, ref, bound, what="gs=8, CUDA-core bar")
 
 
-def test_prefill_requires_workspace():
+def test_prefill_requires_workspace(kernel):
     M, N, K, gs = 64, 128, 256, 64
     need = qg.workspace_size(qg.QG_OP_AFFINE, M, N, K, gs, 0)
     assert need >= M * K * 2  # at least the fp16 copy of x
