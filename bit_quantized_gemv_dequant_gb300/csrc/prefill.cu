@@ -231,6 +231,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
     __shared__ float amax_s;
     __shared__ float tile[2][32][33];
     const int t = threadIdx.x;
+    // fold_kernel is launched as a programmatic dependent of this kernel: it
+    // may start its prologue now and waits for this grid before reading.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((int)blockIdx.x >= Mp) {
         const int tiles_g = (G + 31) / 32;
         const int tb = blockIdx.x - Mp;
@@ -270,10 +273,24 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
     }
     const float4* xr = reinterpret_cast<const float4*>(x + (size_t)m * K);
     const int quads = K >> 2;
+    // Rows of up to kCacheQ * 1024 floats stay in registers between the two
+    // passes (one read of x); longer rows are read twice.
+    constexpr int kCacheQ = 8;
+    const bool cached = quads <= kCacheQ * kPrepThreads;
+    float4 cache[kCacheQ];
     float amax = 0.f;
-    for (int c = t; c < quads; c += kPrepThreads) {
-        const float4 v = __ldg(xr + c);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    auto amax4 = [](float4 v) {
+        return fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    };
+    if (cached) {
+#pragma unroll
+        for (int j = 0; j < kCacheQ; ++j) {
+            const int c = t + j * kPrepThreads;
+            cache[j] = c < quads ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            amax = fmaxf(amax, amax4(cache[j]));
+        }
+    } else {
+        for (int c = t; c < quads; c += kPrepThreads) amax = fmaxf(amax, amax4(__ldg(xr + c)));
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -301,11 +318,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
     const int width = min(gs >> 2, 32);
     const int groups_per_pass = (4 * kPrepThreads) / gs;  // 0 when gs > 1024 (not allowed)
     __half2* xo = reinterpret_cast<__half2*>(xh + (size_t)m * K);
-    for (int base = 0; base < quads; base += kPrepThreads) {
+    // One pass of kPrepThreads float4s starting at element 4 * base; v is this
+    // thread's float4 (ignored past the row's end).
+    auto pass = [&](int base, float4 v) {
         const int c = base + t;
         float f = 0.f;
         if (c < quads) {
-            const float4 v = __ldg(xr + c);
             const __half2 h0 = __floats2half2_rn(v.x * scale, v.y * scale);
             const __half2 h1 = __floats2half2_rn(v.z * scale, v.w * scale);
             xo[2 * c] = h0;
@@ -330,6 +348,18 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
                 if (xsum && g < G) xsum[(size_t)g * Mp + m] = s;
             }
             __syncthreads();
+        }
+    };
+    if (cached) {
+#pragma unroll
+        for (int j = 0; j < kCacheQ; ++j) {
+            if (j * kPrepThreads >= quads) break;  // uniform over the block
+            pass(j * kPrepThreads, cache[j]);
+        }
+    } else {
+        for (int base = 0; base < quads; base += kPrepThreads) {
+            const int c = base + t;
+            pass(base, c < quads ? __ldg(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f));
         }
     }
 }
@@ -376,16 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty(i), 1);
         }
         for (int i = 0; i < kABufs; ++i) {
-            mbar_init(a_full(i), 128);
+            mbar_init(a_full(i), 4);  // one arrival per converter warp
             mbar_init(a_empty(i), 1);
         }
         for (int i = 0; i < kPBufs; ++i) {
             mbar_init(p_full(i), 1);
-            mbar_init(p_empty(i), kEpiWarps * 32);
+            mbar_init(p_empty(i), kEpiWarps);  // one arrival per epilogue warp
         }
         for (int i = 0; i < kXSlots; ++i) {
             mbar_init(x_full(i), 1);
-            mbar_init(x_empty(i), kEpiWarps * 32);
+            mbar_init(x_empty(i), kEpiWarps);
         }
         mbar_init(done_bar, 1);
         fence_mbar_init();
@@ -551,8 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++groups;
                 if (++pb == kPBufs) { pb = 0; pph ^= 1; }
             }
+            // One arrival per warp: the barrier sees 4 arrivals instead of 128
+            // serialised ones. The warp's tensor-memory stores are ordered
+            // before it by the fence and the warp barrier.
             tc_fence_before();
-            mbar_arrive(a_full(ab));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full(ab));
             if (++st == kStages) { st = 0; fph ^= 1; }
             if (++ab == kABufs) { ab = 0; aph ^= 1; }
             if (GK == 4 && ++gst == p.spgs) gst = 0;
@@ -624,8 +658,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (hf + 1 == kChunks) {
                     // Everything of group j is read: release P and the sums.
                     tc_fence_before();
-                    mbar_arrive(p_empty(pb));
-                    mbar_arrive(x_empty(xsl));
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(p_empty(pb));
+                        mbar_arrive(x_empty(xsl));
+                    }
                 }
                 fma_chunk(hf, cur, xv, s2, b2);
                 if (hf + 1 < kChunks) tmem_wait16(nxt);
@@ -767,7 +804,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             mbar_init(empty(i), 1);
         }
         for (int i = 0; i < kFABufs; ++i) {
-            mbar_init(a_full(i), kFStageWarps * 32);
+            mbar_init(a_full(i), kFStageWarps);  // one arrival per converter warp
             mbar_init(a_empty(i), 1);
         }
         mbar_init(done_bar, 1);
@@ -784,6 +821,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Everything below reads what the prep kernel wrote (launched as its
+    // programmatic dependent, this grid may have started before it finished).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == kFProducer) {
         // ------------------------------------------------------------ producer
@@ -926,8 +966,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             tmem_st16(tmem + lane_base + kFACol0 + ab * 32 + h * 16, o);
             tmem_st_wait();
+            // One arrival per warp (8 per stage rather than 256 serialised
+            // ones), after the fence and the warp barrier that order the
+            // warp's tensor-memory stores before it.
             tc_fence_before();
-            mbar_arrive(a_full(ab));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full(ab));
         }
         // Epilogue: this warp's 32 activation rows (columns (w / 4) * 32 ..) of its lanes.
         if (ok && warp_wait(done_bar, 0)) {
@@ -1031,8 +1075,19 @@ int launch_fold(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx,
         if (e != cudaSuccess) return cuda_fail(e);
         configured[dc.device] = 1;
     }
-    kern<<<grid, kFThreads, smem, s>>>(mq, mx, kp);
-    cudaError_t e = cudaGetLastError();
+    // Programmatic dependent of the prep kernel: the prologue (barriers,
+    // tensor memory) overlaps the prep's tail.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mx, kp);
     return e == cudaSuccess ? QG_OK : cuda_fail(e);
 }
 
