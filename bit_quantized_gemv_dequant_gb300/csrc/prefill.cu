@@ -215,6 +215,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// warp_wait for warps that run ahead of the MMA issuer (fold_kernel's
+// converters): suspended while waiting, so that they do not take issue
+// slots from the one thread that issues the MMAs.
+__device__ __forceinline__ bool warp_wait_sleep(uint32_t bar, uint32_t parity) {
+    const bool ok = mbar_wait_sleep(bar, parity);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // ------------------------------------------------------------- prep kernel
 // Blocks [0, Mp) prepare activation rows (with xsum = nullptr, no group
 // sums). The blocks after them transpose 32 x 32 tiles of the scales and
@@ -726,18 +734,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 //               (barrier wait, shared-memory loads, conversion, tensor-memory
 //               store and its wait).
 //   warp 16     TMA producer (codes and xh tiles, as in mma_kernel).
-//   warp 17     MMA issuer: four K = 16 MMAs per stage into one accumulator.
+//   warps 17-18 MMA issuers: warp 17 + p issues the four K = 16 MMAs of the
+//               stages of parity p into accumulator p. A single issuing
+//               thread spends a fixed ~0.25 us per stage (barrier wait,
+//               commit, first MMA) whatever the MMA size, which made it the
+//               bound of the whole tile; two threads on two schedulers halve
+//               that. The epilogue adds the two accumulators.
 constexpr int kFStages = 8;
 constexpr int kFABufs = 8;              // A buffers, 32 columns each
-constexpr int kFAcc = 0;                // accumulator columns [0, kTileT)
-constexpr int kFACol0 = kTileT;         // A buffers: columns [128, 384)
+constexpr int kFAcc = 0;                // accumulator p: columns [p * kTileT, (p + 1) * kTileT)
+constexpr int kFACol0 = 2 * kTileT;     // A buffers: columns [256, 512)
 constexpr int kFConv = 16;              // converter / epilogue warps
 constexpr int kFStageWarps = 8;         // converter warps per stage
 constexpr int kFProducer = kFConv;
-constexpr int kFMma = kFConv + 1;
-constexpr int kFThreads = (kFConv + 2) * 32;
+constexpr int kFMma = kFConv + 1;       // and kFMma + 1
+constexpr int kFThreads = (kFConv + 3) * 32;
 static_assert(kFACol0 + kFABufs * 32 <= kTmemCols, "tensor memory columns");
-static_assert(kFStages % 2 == 0 && kFABufs % 2 == 0, "stage parities own disjoint buffers");
+static_assert(kFStages % 2 == 0, "stage parities own disjoint buffers");
+static_assert(kFABufs == kFStages, "stage i uses shared-memory stage and A buffer i % kFStages");
 
 template <bool PACKED>
 struct GeoF {
@@ -785,9 +799,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t bars = base + Gm::kBarOff;
     auto full = [&](int i) { return bars + 8u * i; };
     auto empty = [&](int i) { return bars + 8u * (kFStages + i); };
+    // empty(i): the MMAs of the stage in slot i are done, so both its shared-
+    // memory stage and its A buffer may be refilled (one commit frees both).
     auto a_full = [&](int i) { return bars + 8u * (2 * kFStages + i); };
-    auto a_empty = [&](int i) { return bars + 8u * (2 * kFStages + kFABufs + i); };
-    constexpr int kDone = 2 * kFStages + 2 * kFABufs;
+    constexpr int kDone = 3 * kFStages;
     const uint32_t done_bar = bars + 8u * kDone;
     static_assert(8 * (kDone + 1) + 4 <= 1024, "barrier area");
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Gm::kBarOff + 8 * (kDone + 1));
@@ -803,11 +818,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
             mbar_init(full(i), 1);
             mbar_init(empty(i), 1);
         }
-        for (int i = 0; i < kFABufs; ++i) {
+        for (int i = 0; i < kFABufs; ++i)
             mbar_init(a_full(i), kFStageWarps);  // one arrival per converter warp
-            mbar_init(a_empty(i), 1);
-        }
-        mbar_init(done_bar, 1);
+        mbar_init(done_bar, 2);  // one commit per MMA issuer
         fence_mbar_init();
     }
     if (warp == kFMma) {
@@ -833,7 +846,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             int issued = 0;
             for (int i = 0; i < nstages; ++i) {
                 const int st = i % kFStages;
-                if (i >= kFStages && !mbar_wait(empty(st), ((i / kFStages) & 1) ^ 1)) {
+                if (i >= kFStages && !mbar_wait_sleep(empty(st), ((i / kFStages) & 1) ^ 1)) {
                     report_error(p.err, DEVERR_TC_WAIT);
                     break;
                 }
@@ -848,28 +861,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (!mbar_wait(full(i % kFStages), (i / kFStages) & 1))
                     report_error(p.err, DEVERR_WAIT_DRAIN);
         }
-    } else if (warp == kFMma) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == kFMma || warp == kFMma + 1) {
+        // --------------------------------------------------------- MMA issuers
         if (lane == 0) {
-            int st = 0, ab = 0;
-            uint32_t aph = 0;
-            for (int i = 0; i < nstages; ++i) {
+            // The loop carries the stage's descriptor and A column as
+            // increments (a descriptor's address field is the byte address
+            // / 16, and no stage address reaches 2^18).
+            const int par = warp - kFMma;
+            const uint64_t d0 = sw128_desc(base);
+            const uint32_t acc = tmem + kFAcc + par * kTileT, a0 = tmem + kFACol0;
+            for (int i = par; i < nstages; i += 2) {
+                const int st = i % kFStages;
                 // a_full implies the stage's copies landed: the converters waited for them.
-                if (!mbar_wait(a_full(ab), aph)) {
+                if (!mbar_wait(a_full(st), (uint32_t)(i / kFStages) & 1u)) {
                     report_error(p.err, DEVERR_TC_WAIT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = base + st * Gm::kStageBytes;
-                const uint32_t aa = tmem + kFACol0 + ab * 32;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    tc_mma_ts(tmem + kFAcc, aa + kk * 8, sw128_desc(sb + kk * 32), kIdesc,
-                              (i | kk) ? 1u : 0u);
+                const uint64_t d = d0 + (uint64_t)(st * (Gm::kStageBytes >> 4));
+                const uint32_t aa = a0 + st * 32;
+                tc_mma_ts(acc, aa, d, kIdesc, i > par ? 1u : 0u);
+                tc_mma_ts(acc, aa + 8, d + 2, kIdesc, 1u);
+                tc_mma_ts(acc, aa + 16, d + 4, kIdesc, 1u);
+                tc_mma_ts(acc, aa + 24, d + 6, kIdesc, 1u);
                 tc_commit(empty(st));
-                tc_commit(a_empty(ab));
-                if (++st == kFStages) st = 0;
-                if (++ab == kFABufs) { ab = 0; aph ^= 1; }
             }
             tc_commit(done_bar);
             if (!mbar_wait(done_bar, 0)) report_error(p.err, DEVERR_WAIT_DRAIN);
@@ -913,13 +928,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
         load_sb(par, nx);
         bool ok = true;
         for (int i = par; i < nstages; i += 2) {
-            const int st = i % kFStages, ab = i % kFABufs;
-            const uint32_t fph = (uint32_t)(i / kFStages) & 1u, aph = (uint32_t)(i / kFABufs) & 1u;
+            const int st = i % kFStages, ab = st;
+            const uint32_t fph = (uint32_t)(i / kFStages) & 1u;
             // Scaled by 2^f only here, one stage after the loads were issued.
             const float2 sA = make_float2(nx[0] * pw, nx[0] * pw), bA = make_float2(nx[1] * pw, nx[1] * pw);
             const float2 sB = make_float2(nx[2] * pw, nx[2] * pw), bB = make_float2(nx[3] * pw, nx[3] * pw);
             if (i + 2 < nstages) load_sb(i + 2, nx);
-            if (!warp_wait(full(st), fph) || (i >= kFABufs && !warp_wait(a_empty(ab), aph ^ 1))) {
+            if (!warp_wait_sleep(full(st), fph) ||
+                (i >= kFStages && !warp_wait_sleep(empty(st), fph ^ 1))) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
                 ok = false;
                 break;
@@ -982,14 +998,21 @@ __global__ void __launch_bounds__(kFThreads, 1)
             float* yp = p.y + (size_t)(m0 + c0) * p.N + (nvalid ? n : 0);
 #pragma unroll
             for (int cb16 = 0; cb16 < 2; ++cb16) {
-                uint32_t r[16];
+                uint32_t r[16], r1[16];
                 tmem_ld16(tmem + lane_base + kFAcc + c0 + cb16 * 16, r);
+                // The odd stages' accumulator (never written when K fits one stage).
+                if (nstages > 1) {
+                    tmem_ld16(tmem + lane_base + kFAcc + kTileT + c0 + cb16 * 16, r1);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r1[j] = 0u;
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int col = cb16 * 16 + j;
                     const float ivm = __shfl_sync(0xFFFFFFFFu, ivl, col);
-                    if (nvalid && m0 + c0 + col < p.M)
-                        yp[(size_t)col * p.N] = (__uint_as_float(r[j]) * ipw) * ivm;
+                    const float a = __uint_as_float(r[j]) + __uint_as_float(r1[j]);
+                    if (nvalid && m0 + c0 + col < p.M) yp[(size_t)col * p.N] = (a * ipw) * ivm;
                 }
             }
         } else if (ok) {

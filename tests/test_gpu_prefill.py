@@ -115,6 +115,8 @@ SHAPES = [
     (33, 70, 2048, 1024),
     (64, 136, 128, 16),
     (20, 150, 96, 32),     # K not a multiple of the 64-wide stage
+    (24, 130, 64, 32),     # a single stage
+    (40, 64, 32, 16),      # a single, partial stage
 ]
 
 
