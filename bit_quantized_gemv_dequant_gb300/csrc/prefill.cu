@@ -239,8 +239,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
     __shared__ float amax_s;
     __shared__ float tile[2][32][33];
     const int t = threadIdx.x;
-    // fold_kernel is launched as a programmatic dependent of this kernel: it
-    // may start its prologue now and waits for this grid before reading.
+    // This kernel is launched as a programmatic dependent of whatever precedes
+    // it on the stream (it may be resident before that kernel ends): it waits
+    // for it before reading or writing anything. fold_kernel, launched as this
+    // kernel's dependent, may then start its prologue; it waits for this grid
+    // before reading what it writes.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((int)blockIdx.x >= Mp) {
         const int tiles_g = (G + 31) / 32;
@@ -837,6 +841,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     // Everything below reads what the prep kernel wrote (launched as its
     // programmatic dependent, this grid may have started before it finished).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next kernel on the stream may become resident now; a dependent
+    // launch of it waits for this grid before touching its data.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kFProducer) {
         // ------------------------------------------------------------ producer
@@ -1087,6 +1094,26 @@ int launch_main(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx, 
     return e == cudaSuccess ? QG_OK : cuda_fail(e);
 }
 
+// prep_kernel as a programmatic dependent of the preceding kernel (it waits
+// for it before touching any data).
+int launch_prep(unsigned blocks, cudaStream_t s, const float* x, __half* xh, float* xsum,
+                float* inv, const float* sc, const float* bi, float* sc_t, float* bi_t,
+                float* bpart, float qmax, int M, int N, int K, int gs, int G, int Mp) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prep_kernel, x, xh, xsum, inv, sc, bi, sc_t, bi_t,
+                                       bpart, qmax, M, N, K, gs, G, Mp);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
 template <bool PACKED, bool GS16>
 int launch_fold(const DevCtx& dc, const CUtensorMap& mq, const CUtensorMap& mx,
                 const FoldParams& kp, dim3 grid, cudaStream_t s) {
@@ -1177,11 +1204,10 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
     const long long tiles = ((a.N + 31) / 32) * (long long)((L.G + 31) / 32);
     if (tiles > 0x7FFFFFFFll - L.Mp) return QG_ERR_UNSUPPORTED;
     if (!launch_option(QG_OPT_PREFILL_EXACT)) {
-        prep_kernel<<<(unsigned)(L.Mp + tiles), kPrepThreads, 0, s>>>(
-            a.x, xh, nullptr, inv, a.scales, a.biases, sc_t, bi_t, bpart,
-            packed ? 15.f : 255.f, (int)a.M, (int)a.N, (int)a.K, a.gs, L.G, L.Mp);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e);
+        int rc2 = launch_prep((unsigned)(L.Mp + tiles), s, a.x, xh, nullptr, inv, a.scales,
+                              a.biases, sc_t, bi_t, bpart, packed ? 15.f : 255.f, (int)a.M,
+                              (int)a.N, (int)a.K, a.gs, L.G, L.Mp);
+        if (rc2 != QG_OK) return rc2;
         FoldParams fp{};
         fp.scales_t = sc_t;
         fp.biases_t = bi_t;
@@ -1201,11 +1227,9 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
         return packed ? launch_fold<true, false>(dc, mq, mx, fp, grid, s)
                       : launch_fold<false, false>(dc, mq, mx, fp, grid, s);
     }
-    prep_kernel<<<(unsigned)(L.Mp + tiles), kPrepThreads, 0, s>>>(
-        a.x, xh, xsum, inv, a.scales, a.biases, sc_t, bi_t, nullptr, 0.f, (int)a.M, (int)a.N,
-        (int)a.K, a.gs, L.G, L.Mp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
+    rc = launch_prep((unsigned)(L.Mp + tiles), s, a.x, xh, xsum, inv, a.scales, a.biases, sc_t,
+                     bi_t, nullptr, 0.f, (int)a.M, (int)a.N, (int)a.K, a.gs, L.G, L.Mp);
+    if (rc != QG_OK) return rc;
 
     Params kp{};
     kp.scales_t = sc_t;
