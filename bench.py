@@ -305,6 +305,11 @@ def sweep_specs():
         # Q4_0 / Q4_K prefill: repacked to affine codes (group 32), tcgen05 MMAs.
         ("prefill dual q4_0 N=K=4096 M=512", lambda: make_dual_q4_0(512, 4096, 4096, 80)),
         ("prefill q4_k N=K=4096 M=512", lambda: make_single("q4_k", 512, 4096, 4096, 81)),
+        # The same prefill calls with the folded-weight kernel (QG_OPT_PREFILL_FOLD).
+        ("cfg3 affine u8 M=512 folded", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 0)),
+        ("cfg3 affine packed M=512 folded", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 1)),
+        ("prefill dual q4_0 N=K=4096 M=512 folded", lambda: make_dual_q4_0(512, 4096, 4096, 80)),
+        ("prefill q4_k N=K=4096 M=512 folded", lambda: make_single("q4_k", 512, 4096, 4096, 81)),
     ]
     for M in (1, 2, 4, 8):
         specs += [
@@ -602,6 +607,7 @@ def main():
         specs = dict(sweep_specs())
         if args.only not in specs:
             ap.error(f"--only: unknown configuration {args.only!r}; one of {sorted(specs)}")
+        qg.set_option(qg.QG_OPT_PREFILL_FOLD, 1 if args.only.endswith("folded") else 0)
         r = specs[args.only]()
         res = measure(r, args.steps, args.warmup)
         res["tflops"] = r.flops / (res["us_per_call"] * 1e6)
@@ -702,7 +708,9 @@ def main():
         torch.cuda.empty_cache()
         specs = sweep_specs()
         for name, mk in specs:
+            fold_old = qg.get_option(qg.QG_OPT_PREFILL_FOLD)
             try:
+                qg.set_option(qg.QG_OPT_PREFILL_FOLD, 1 if name.endswith("folded") else 0)
                 r = mk()
                 steps = args.sweep_steps if "512" not in name else max(20, args.sweep_steps // 20)
                 res = measure(r, steps, 5, repeats=20)
@@ -718,6 +726,8 @@ def main():
                 torch.cuda.empty_cache()
             except Exception as e:  # report, keep going
                 sweep[name] = {"error": str(e)[:200]}
+            finally:
+                qg.set_option(qg.QG_OPT_PREFILL_FOLD, fold_old)
         out["sweep"] = sweep
         if qg.device_error():
             raise RuntimeError("device error word set during the sweep")

@@ -1203,7 +1203,7 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
     const dim3 grid(L.Mp / kTileT, (unsigned)((a.N + kTileN - 1) / kTileN));
     const long long tiles = ((a.N + 31) / 32) * (long long)((L.G + 31) / 32);
     if (tiles > 0x7FFFFFFFll - L.Mp) return QG_ERR_UNSUPPORTED;
-    if (!launch_option(QG_OPT_PREFILL_EXACT)) {
+    if (launch_option(QG_OPT_PREFILL_FOLD)) {
         int rc2 = launch_prep((unsigned)(L.Mp + tiles), s, a.x, xh, nullptr, inv, a.scales,
                               a.biases, sc_t, bi_t, bpart, packed ? 15.f : 255.f, (int)a.M,
                               (int)a.N, (int)a.K, a.gs, L.G, L.Mp);

@@ -29,7 +29,7 @@ std::atomic<long long> g_opt_stream_warps{0};
 std::atomic<long long> g_opt_stream_slots{0};
 std::atomic<long long> g_opt_ahead{2};
 std::atomic<long long> g_opt_staged_warps{0};
-std::atomic<long long> g_opt_prefill_exact{0};
+std::atomic<long long> g_opt_prefill_fold{0};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -157,7 +157,7 @@ long long launch_option(int option) {
         case QG_OPT_STREAM_SLOTS: return g_opt_stream_slots.load(std::memory_order_relaxed);
         case QG_OPT_STAGES_AHEAD: return g_opt_ahead.load(std::memory_order_relaxed);
         case QG_OPT_STAGED_WARPS: return g_opt_staged_warps.load(std::memory_order_relaxed);
-        case QG_OPT_PREFILL_EXACT: return g_opt_prefill_exact.load(std::memory_order_relaxed);
+        case QG_OPT_PREFILL_FOLD: return g_opt_prefill_fold.load(std::memory_order_relaxed);
         default: return 0;
     }
 }
@@ -368,9 +368,9 @@ int qg_set_option(int option, int64_t value) {
             if (value != 0 && value != 8) return QG_ERR_INVALID_ARG;
             g_opt_staged_warps.store(value, std::memory_order_relaxed);
             return QG_OK;
-        case QG_OPT_PREFILL_EXACT:
+        case QG_OPT_PREFILL_FOLD:
             if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
-            g_opt_prefill_exact.store(value, std::memory_order_relaxed);
+            g_opt_prefill_fold.store(value, std::memory_order_relaxed);
             return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
@@ -394,8 +394,8 @@ int qg_get_option(int option, int64_t* value) {
         case QG_OPT_STAGED_WARPS:
             *value = g_opt_staged_warps.load(std::memory_order_relaxed);
             return QG_OK;
-        case QG_OPT_PREFILL_EXACT:
-            *value = g_opt_prefill_exact.load(std::memory_order_relaxed);
+        case QG_OPT_PREFILL_FOLD:
+            *value = g_opt_prefill_fold.load(std::memory_order_relaxed);
             return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }

@@ -232,16 +232,17 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * registers and shared memory, so that the next launch's CTA can be resident
  * beside this one (tuning). */
 /*
- * QG_OPT_PREFILL_EXACT (default 0; or 1): which tensor-core prefill kernel
- * qmm_affine (and the Q4_0/Q4_K prefill built on it) runs. 0: scale and bias
- * folded into fp16 weights, w' = fp16((s q + b) 2^f_n) with a power of two
- * per weight row, one f32 accumulator over all of K. 1: exact integer codes
- * on the tensor cores and scale and bias applied per group in an f32
- * epilogue. Both stay within 2e-3 * sum_k |x w|; 1 keeps the weights exact
- * whatever the spread of the scales within a row, 0 is faster. */
+ * QG_OPT_PREFILL_FOLD (default 0; or 1): which tensor-core prefill kernel
+ * qmm_affine (and the Q4_0/Q4_K prefill built on it) runs. 0: exact integer
+ * codes on the tensor cores, scale and bias applied per group in an f32
+ * epilogue. 1: scale and bias folded into fp16 weights,
+ * w' = fp16((s q + b) 2^f_n) with a power of two per weight row, one f32
+ * accumulator over all of K, faster. Both stay within 2e-3 * sum_k |x w|
+ * for weight rows whose scales span less than 2^29; 0 keeps the weights
+ * exact whatever their spread. */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
        QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6, QG_OPT_STAGED_WARPS = 7,
-       QG_OPT_PREFILL_EXACT = 8 };
+       QG_OPT_PREFILL_FOLD = 8 };
 QG_API int qg_set_option(int option, int64_t value);
 QG_API int qg_get_option(int option, int64_t* value);
 

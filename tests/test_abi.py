@@ -88,7 +88,7 @@ def test_launch_options_round_trip_and_validation(lib):
              5: ([0, 2, 8], [1, 9]),          # QG_OPT_STREAM_SLOTS
              6: ([0, 1, 64], [65, -1]),       # QG_OPT_STAGES_AHEAD
              7: ([0, 8], [4, 16]),            # QG_OPT_STAGED_WARPS
-             8: ([0, 1], [2, -1])}            # QG_OPT_PREFILL_EXACT
+             8: ([0, 1], [2, -1])}            # QG_OPT_PREFILL_FOLD
     for opt, (good, bad) in cases.items():
         rc, old = get(opt)
         assert rc == 0

@@ -7,9 +7,9 @@ path's one approximation: rounding each activation row, scaled by a power of
 two, to fp16. Feeding those rounded activations to the oracle must reproduce
 y within the f32 bar (1e-5), so no other error source (a wrong group, scale,
 bias or tile) can hide inside the looser tolerance. The folded-weight kernel
-(the default) also rounds each weight row, scaled by a power of two, to fp16;
-its tighter check feeds the oracle both rounded operands. Every tensor-core
-test runs on both kernels (QG_OPT_PREFILL_EXACT 0 and 1).
+(QG_OPT_PREFILL_FOLD = 1) also rounds each weight row, scaled by a power of
+two, to fp16; its tighter check feeds the oracle both rounded operands. Every
+tensor-core test runs on both kernels.
 
 Shapes span several 128x128 tiles with ragged tails in M, N and K, every
 group size the path takes (16 .. 1024), both code storages, 8-bit codes, and
@@ -39,12 +39,13 @@ def min_m():
     qg.set_option(qg.QG_OPT_PREFILL_MIN_M, old)
 
 
-@pytest.fixture(params=[0, 1], ids=["fold", "exact"])
+@pytest.fixture(params=["exact", "fold"])
 def kernel(request):
-    old = qg.get_option(qg.QG_OPT_PREFILL_EXACT)
-    qg.set_option(qg.QG_OPT_PREFILL_EXACT, request.param)
-    yield request.param
-    qg.set_option(qg.QG_OPT_PREFILL_EXACT, old)
+    """Selects the prefill kernel; the value is true for the exact-code one."""
+    old = qg.get_option(qg.QG_OPT_PREFILL_FOLD)
+    qg.set_option(qg.QG_OPT_PREFILL_FOLD, int(request.param == "fold"))
+    yield request.param == "exact"
+    qg.set_option(qg.QG_OPT_PREFILL_FOLD, old)
 
 
 def _run(c, gs, packed, M=None):
