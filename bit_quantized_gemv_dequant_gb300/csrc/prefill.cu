@@ -621,9 +621,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* brow = p.biases_t + (nvalid ? n : 0);
         int pb = 0, xsl = 0;
         uint32_t pph = 0, xph = 0;
-        // Scale and bias of the next group are loaded one group ahead.
-        float s_nx = nvalid ? __ldg(srow) : 0.f;
-        float b_nx = nvalid ? __ldg(brow) : 0.f;
+        // Scales and biases are loaded kAhead groups ahead (a group takes well
+        // under an L2 round trip), in a register queue shifted once per group.
+        constexpr int kAhead = 4;
+        float sq[kAhead], bq[kAhead];
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            sq[u] = (nvalid && u < p.G) ? __ldg(srow + (size_t)u * p.N) : 0.f;
+            bq[u] = (nvalid && u < p.G) ? __ldg(brow + (size_t)u * p.N) : 0.f;
+        }
         // acc[c] (tokens 2c, 2c+1 of this warp's kEpiCols) += s * P + b * X for
         // one 16-column chunk hf of P.
         auto fma_chunk = [&](int hf, const uint32_t (&r)[16], const float4 (&xv)[4], float2 s2,
@@ -640,11 +646,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         for (int j = 0; j < p.G; ++j) {
-            const float2 s2 = make_float2(s_nx, s_nx), b2 = make_float2(b_nx, b_nx);
-            if (nvalid && j + 1 < p.G) {
-                s_nx = __ldg(srow + (size_t)(j + 1) * p.N);
-                b_nx = __ldg(brow + (size_t)(j + 1) * p.N);
+            const float2 s2 = make_float2(sq[0], sq[0]), b2 = make_float2(bq[0], bq[0]);
+#pragma unroll
+            for (int u = 0; u + 1 < kAhead; ++u) {
+                sq[u] = sq[u + 1];
+                bq[u] = bq[u + 1];
             }
+            const bool more = nvalid && j + kAhead < p.G;
+            sq[kAhead - 1] = more ? __ldg(srow + (size_t)(j + kAhead) * p.N) : 0.f;
+            bq[kAhead - 1] = more ? __ldg(brow + (size_t)(j + kAhead) * p.N) : 0.f;
             if (!warp_wait(p_full(pb), pph) || !warp_wait(x_full(xsl), xph)) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
                 ok = false;
