@@ -305,9 +305,11 @@ SPlan make_stream_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float*
     sp.ok = false;
     const long long mode = launch_option(QG_OPT_STREAM);
     if (Mc > 2 || mode == 0) return sp;
-    // Automatic: the formats for which it measured faster than the staged
-    // kernel on GB300 (Q4_K); 2 takes it for every eligible call.
-    if (mode == 1 && a.fmt != FMT_Q4_K) return sp;
+    // Automatic: where it measured faster than the staged kernel on GB300:
+    // Q4_K, except two input rows with K above 8192 (FFN down, K = 12288:
+    // 21.4 us against 19.4 us). 2 takes it for every eligible call. The
+    // choice depends on the format, the rows and K only, never on N.
+    if (mode == 1 && (a.fmt != FMT_Q4_K || (Mc == 2 && a.K > 8192))) return sp;
     const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
     if (a.K % 256) return sp;
     const long long U = a.K / 256;

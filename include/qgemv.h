@@ -208,7 +208,8 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
 /*
  * QG_OPT_STREAM (default 1): which GEMV/qmm calls with M <= 2 (per slice of
  * x) take the streaming kernel instead of the staged-stage kernel. 0: none.
- * 1: the formats for which it is the faster of the two (Q4_K). 2: every
+ * 1: where it is the faster of the two (Q4_K, except two rows with
+ * K > 8192). 2: every
  * eligible call. Eligible: K % 256 == 0, (K / 256) % 4 == 0, the weight, x
  * (and affine scale/bias) pointers 16-byte aligned and, for affine weights,
  * group_size >= 32. Both kernels give results within the same tolerance; the
