@@ -1,5 +1,8 @@
 // Affine-quantized matmul for many activation rows (prefill) on the fifth-
-// generation tensor cores.
+// generation tensor cores: the prep kernel, the exact-code kernel (the
+// default) and the host side of both kernels. The folded-weight kernel
+// (QG_OPT_PREFILL_FOLD = 1) is in prefill_fold.cu, the pieces both share in
+// prefill_common.cuh.
 //
 // Page: qmm_affine.rs (mlx-native 0.21.1), dispatch_qmm_affine_t_f32 and the
 // packed 4-bit variant: y[m,n] = sum_k x[m,k] * w[n,k], w[n,k] = s[n,g] *
@@ -30,9 +33,12 @@
 //                      converted weights never pass through shared memory.
 //         warp 13      MMA issuer: kind::f16, M=128 (weight rows), N=128
 //                      (activation rows), K=16 per instruction, f32
-//                      accumulators P_g in tensor memory, two buffers.
+//                      accumulators P_g in tensor memory, three buffers.
 //         warps 4-11   epilogue: acc += s * P_g + b * X_g per group, in f32
-//                      registers; at the end y = acc * 2^-e_m.
+//                      registers (scales and biases read four groups
+//                      ahead); at the end y = acc * 2^-e_m. A converter fills
+//                      group i's A buffer only once the epilogue has released
+//                      P buffer i - 3: that cycle bounds the kernel.
 // Every wait is bounded; a wait that runs out records an error bit and the
 // CTA winds down (drains its copies and MMAs, frees tensor memory) instead of
 // hanging.
