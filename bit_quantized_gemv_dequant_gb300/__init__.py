@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_MISALIGNED = 0, 1, 2, 3
 QG_ERR_CUDA, QG_ERR_WORKSPACE, QG_ERR_DEVICE = 4, 5, 6
-QG_OP_Q4_0, QG_OP_DUAL_Q4_0, QG_OP_Q4_K, QG_OP_AFFINE = 0, 1, 2, 3
+QG_OP_Q4_0, QG_OP_DUAL_Q4_0, QG_OP_Q4_K, QG_OP_AFFINE, QG_OP_AF4_G64 = 0, 1, 2, 3, 4
 QG_OPT_PDL = 1
 QG_OPT_PREFILL_MIN_M = 2
 QG_OPT_STREAM, QG_OPT_STREAM_WARPS, QG_OPT_STREAM_SLOTS = 3, 4, 5
@@ -35,7 +35,7 @@ EXPORTS = ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_spl
            "dequant_q4_0", "dequant_q4_k", "dequant_affine", "qg_workspace_size",
            "qg_status_string", "qg_last_cuda_error", "qg_device_error",
            "qg_selftest_wait_timeout", "qg_set_option", "qg_get_option",
-           "qgemv_q4_k_noalloc")
+           "qgemv_q4_k_noalloc", "qg_prepare_af4_g64", "qmm_af4_g64")
 
 _LIB = None
 _LOCK = threading.Lock()
@@ -79,6 +79,8 @@ def lib():
             "qg_set_option": [I, I64],
             "qg_get_option": [I, C.POINTER(I64)],
             "qgemv_q4_k_noalloc": [P, P, P, I64, I64, I64, P],
+            "qg_prepare_af4_g64": [P, P, P, P, P, I64, I64, P],
+            "qmm_af4_g64": [P, P, P, P, I64, I64, I64, P, SZ, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -207,6 +209,32 @@ def qmm_affine(x, q, scales, biases, group_size, packed, y=None, *, workspace=No
                             _dev(biases, "biases", torch.float32), _dev(y, "y", torch.float32),
                             M, N, K, int(group_size), int(packed), ws, wsb, _stream(stream)),
            "qmm_affine")
+    return y
+
+
+def prepare_af4_g64(codes, scales, biases, *, stream=None):
+    """(plane, metadata) of the prepared AF4-g64 layout (int32 tensors holding
+    the u32 words): codes uint8 [N, K] (0..15), scales and biases bfloat16
+    [N, K/64]."""
+    N, K = codes.shape
+    plane = torch.empty(N * K // 8, dtype=torch.int32, device=codes.device)
+    meta = torch.empty(N * K // 64, dtype=torch.int32, device=codes.device)
+    _check(lib().qg_prepare_af4_g64(_dev(codes, "codes", torch.uint8),
+                                    _dev(scales, "scales", torch.bfloat16),
+                                    _dev(biases, "biases", torch.bfloat16), plane.data_ptr(),
+                                    meta.data_ptr(), N, K, _stream(stream)), "qg_prepare_af4_g64")
+    return plane, meta
+
+
+def qmm_af4_g64(x, plane, metadata, N, y=None, *, workspace=None, stream=None):
+    """y[M,N] = x[M,K] . w^T from the prepared AF4-g64 layout (M <= 32)."""
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(QG_OP_AF4_G64, M, N, K, 0, 0, x.device, workspace)
+    _check(lib().qmm_af4_g64(_dev(x, "x", torch.float32), _dev(plane, "plane", torch.int32),
+                             _dev(metadata, "metadata", torch.int32), _dev(y, "y", torch.float32),
+                             M, N, K, ws, wsb, _stream(stream)), "qmm_af4_g64")
     return y
 
 

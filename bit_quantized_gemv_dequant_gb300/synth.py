@@ -181,5 +181,20 @@ def affine_case(case: int, N: int, K: int, M: int, gs: int) -> dict:
             "x": normal(1000 * case + T_X, (M, K))}
 
 
+def bf16_bits(v: np.ndarray) -> np.ndarray:
+    """f32 -> bfloat16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def af4_case(case: int, N: int, K: int, M: int) -> dict:
+    """AF4-g64 inputs: codes U{0..15}, bf16 scales ~ U(0.001, 0.01) and
+    biases ~ U(-0.08, 0) per 64-group (as bit patterns), x ~ N(0, 1)."""
+    return {"q": codes(1000 * case + T_Q, (N, K)),
+            "s_bits": bf16_bits(uniform(1000 * case + T_S, (N, K // 64), 0.001, 0.01)),
+            "b_bits": bf16_bits(uniform(1000 * case + T_B, (N, K // 64), -0.08, 0.0)),
+            "x": normal(1000 * case + T_X, (M, K))}
+
+
 def qkv_case(case: int, seq: int, q_sp: int, k_sp: int, v_sp: int) -> np.ndarray:
     return normal(1000 * case + T_QKV, (seq, q_sp + k_sp + v_sp))

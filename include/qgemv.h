@@ -86,7 +86,8 @@ enum {
     QG_OP_Q4_0 = 0,
     QG_OP_DUAL_Q4_0 = 1,
     QG_OP_Q4_K = 2,
-    QG_OP_AFFINE = 3
+    QG_OP_AFFINE = 3,
+    QG_OP_AF4_G64 = 4
 };
 
 /* Single Q4_0 projection: y[M,N] = x[M,K] . dequant(w)[N,K]^T.
@@ -185,6 +186,37 @@ QG_API int dequant_q4_0(const void* w, float* out, int64_t N, int64_t K, qg_stre
 QG_API int dequant_q4_k(const void* w, float* out, int64_t N, int64_t K, qg_stream_t stream);
 QG_API int dequant_affine(const void* q, const float* scales, const float* biases, float* out,
                    int64_t N, int64_t K, int group_size, int packed, qg_stream_t stream);
+
+/* The prepared 4-bit affine layout with groups of 64 ("AF4-g64").
+ * Page: qmm_affine.rs (mlx-native 0.21.1), prepare_af4_g64 (test module) and
+ * dispatch_qmm_affine_t_packed_simd4_b4_gs64_bf16. N % 64 == 0, K % 64 == 0.
+ *  - plane: u32 [N/64][K/32][64][4]. Word c (0..3) of (row r, 32-group g)
+ *    holds codes of row r at k = 32g + e: for pair p = 0..3, with
+ *    e0 = 16 (p >> 1) + 4c + 2 (p & 1), code e0 in bits 4p..4p+3 and code
+ *    e0 + 1 in bits 16 + 4p..19 + 4p.
+ *  - metadata: u32 [N/64][K/64][64]: bf16 scale | bf16 bias << 16 of
+ *    (row, 64-group).
+ * The weight is w = scale * q + bias, with the bf16 values taken exactly as
+ * f32 and one f32 rounding (as qmm_affine).
+ *
+ * qg_prepare_af4_g64 writes plane and metadata from codes (u8 [N, K], values
+ * 0..15) and the bf16 bits of scales and biases (u16 [N, K/64]). A bit
+ * rearrangement: the result is exact.
+ *
+ * qmm_af4_g64: y[M,N] = x[M,K] . w[N,K]^T from the prepared layout, M <= 32
+ * (the page's limit). The page's kernel rounds x to bf16 (error class:
+ * relative RMS and max |err| / max(|y|, 1) <= 5e-3). Here the prepared layout
+ * is unpacked into the workspace as packed affine codes with f32 scales and
+ * biases and qmm_affine runs on it, so the result is qmm_affine's: within
+ * 1e-5 * sum_k |x w| for M < QG_OPT_PREFILL_MIN_M, 2e-3 * sum_k |x w| on the
+ * tensor cores. Needs qg_workspace_size(QG_OP_AF4_G64, M, N, K, 0, 0)
+ * bytes. plane, metadata and workspace 16-byte aligned. */
+QG_API int qg_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales_bf16,
+                              const uint16_t* biases_bf16, uint32_t* plane, uint32_t* metadata,
+                              int64_t N, int64_t K, qg_stream_t stream);
+QG_API int qmm_af4_g64(const float* x, const uint32_t* plane, const uint32_t* metadata, float* y,
+                       int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                       qg_stream_t stream);
 
 /* Workspace bytes op (QG_OP_*) needs for the given shape; *bytes = 0 when
  * none. group_size/packed matter only for QG_OP_AFFINE. Returns a status. */

@@ -58,6 +58,13 @@ def _bind(path: str):
     L.orc_gemv_dual_q4_0.restype = C.c_int
     L.orc_qkv_split.argtypes = [_u32p, _u32p, _u32p, _u32p, _i64, _i64, _i64, _i64]
     L.orc_qkv_split.restype = None
+    _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+    L.orc_prepare_af4_g64.argtypes = [_u8p, _u16p, _u16p, _i64, _i64, _u32p, _u32p]
+    L.orc_prepare_af4_g64.restype = None
+    L.orc_af4_unpack.argtypes = [_u32p, _u32p, _i64, _i64, _u8p, _u16p, _u16p]
+    L.orc_af4_unpack.restype = None
+    L.orc_bf16_to_float.argtypes = [C.c_uint16]
+    L.orc_bf16_to_float.restype = C.c_float
     return L
 
 
@@ -188,6 +195,43 @@ def qmm_affine(x, q, s, b, M: int, N: int, K: int, gs: int, packed: bool, rows=N
                                 _c(s, np.float32).ravel(), _c(b, np.float32).ravel(), M, N, K, gs,
                                 int(bool(packed)), rp, nr, ref, bound))
     return ref, bound
+
+
+# ---------------------------------------------------------------- AF4-g64
+def prepare_af4_g64(codes, scales_bits, biases_bits, N: int, K: int):
+    """(plane u32 [N*K/8], meta u32 [N*K/64]) of the prepared layout."""
+    plane = np.zeros(N * K // 8, dtype=np.uint32)
+    meta = np.zeros(N * K // 64, dtype=np.uint32)
+    lib().orc_prepare_af4_g64(_c(codes, np.uint8).ravel(), _c(scales_bits, np.uint16).ravel(),
+                              _c(biases_bits, np.uint16).ravel(), N, K, plane, meta)
+    return plane, meta
+
+
+def af4_unpack(plane, meta, N: int, K: int):
+    """(codes u8 [N, K], scale bits u16 [N, K/64], bias bits u16 [N, K/64])."""
+    codes = np.zeros((N, K), dtype=np.uint8)
+    sb = np.zeros((N, K // 64), dtype=np.uint16)
+    bb = np.zeros((N, K // 64), dtype=np.uint16)
+    lib().orc_af4_unpack(_c(plane, np.uint32).ravel(), _c(meta, np.uint32).ravel(), N, K,
+                         codes.reshape(-1), sb.reshape(-1), bb.reshape(-1))
+    return codes, sb, bb
+
+
+def bf16_to_float_array(bits) -> np.ndarray:
+    f = lib().orc_bf16_to_float
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    out = np.empty(flat.size, dtype=np.float32)
+    for i, h in enumerate(flat.tolist()):
+        out[i] = f(h)
+    return out.reshape(np.shape(bits))
+
+
+def qmm_af4_g64(x, codes, scales_bits, biases_bits, M: int, N: int, K: int, rows=None):
+    """The AF4-g64 qmm from its unprepared definition: qmm_affine with group
+    size 64 and the bf16 scales and biases taken exactly as f32."""
+    s = bf16_to_float_array(scales_bits)
+    b = bf16_to_float_array(biases_bits)
+    return qmm_affine(x, codes, s, b, M, N, K, 64, False, rows=rows)
 
 
 def qkv_split(qkv, seq: int, q_sp: int, k_sp: int, v_sp: int):

@@ -292,3 +292,65 @@ ORC_API void orc_qkv_split(const uint32_t* qkv, uint32_t* q, uint32_t* k, uint32
         for (int64_t j = 0; j < v_sp; ++j) v[t * v_sp + j] = row[q_sp + k_sp + j];
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* The prepared AF4-g64 layout. Page: qmm_affine.rs (mlx-native 0.21.1),     */
+/* prepare_af4_g64 in the test module, written out here as the definition:  */
+/*   plane[((r / 64) * K/32 + g) * 64 + r % 64][c] (g: 32-wide group, c: 0..3)*/
+/*   holds, for each pair p = 0..3 with e = 32 g + 16 (p / 2) + 4 c + 2 (p % 2),*/
+/*   code[r][e] in bits 4p.. and code[r][e + 1] in bits 16 + 4p..;           */
+/*   meta[((r / 64) * K/64 + h) * 64 + r % 64] = scale bits | bias bits << 16 */
+/*   for the 64-wide group h.                                                */
+/* Parity pins: a hand-computed word (tests/golden/af4_g64.txt) and the      */
+/* round trip through orc_af4_unpack.                                        */
+/* ------------------------------------------------------------------------ */
+ORC_API void orc_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales,
+                                 const uint16_t* biases, int64_t N, int64_t K, uint32_t* plane,
+                                 uint32_t* meta) {
+    const int64_t g32n = K / 32, g64n = K / 64;
+    for (int64_t r = 0; r < N; ++r) {
+        for (int64_t h = 0; h < g64n; ++h)
+            meta[((r / 64) * g64n + h) * 64 + r % 64] =
+                (uint32_t)scales[r * g64n + h] | ((uint32_t)biases[r * g64n + h] << 16);
+        for (int64_t g = 0; g < g32n; ++g)
+            for (int c = 0; c < 4; ++c) {
+                uint32_t word = 0;
+                for (int p = 0; p < 4; ++p) {
+                    const int64_t e = g * 32 + 16 * (p / 2) + 4 * c + 2 * (p % 2);
+                    word |= (uint32_t)(codes[r * K + e] & 15u) << (4 * p);
+                    word |= (uint32_t)(codes[r * K + e + 1] & 15u) << (16 + 4 * p);
+                }
+                plane[(((r / 64) * g32n + g) * 64 + r % 64) * 4 + c] = word;
+            }
+    }
+}
+
+/* The inverse: codes [N, K] and the bf16 bits back from plane and meta. */
+ORC_API void orc_af4_unpack(const uint32_t* plane, const uint32_t* meta, int64_t N, int64_t K,
+                            uint8_t* codes, uint16_t* scales, uint16_t* biases) {
+    const int64_t g32n = K / 32, g64n = K / 64;
+    for (int64_t r = 0; r < N; ++r) {
+        for (int64_t h = 0; h < g64n; ++h) {
+            const uint32_t m = meta[((r / 64) * g64n + h) * 64 + r % 64];
+            scales[r * g64n + h] = (uint16_t)(m & 0xFFFFu);
+            biases[r * g64n + h] = (uint16_t)(m >> 16);
+        }
+        for (int64_t g = 0; g < g32n; ++g)
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t word = plane[(((r / 64) * g32n + g) * 64 + r % 64) * 4 + c];
+                for (int p = 0; p < 4; ++p) {
+                    const int64_t e = g * 32 + 16 * (p / 2) + 4 * c + 2 * (p % 2);
+                    codes[r * K + e] = (uint8_t)((word >> (4 * p)) & 15u);
+                    codes[r * K + e + 1] = (uint8_t)((word >> (16 + 4 * p)) & 15u);
+                }
+            }
+    }
+}
+
+/* bfloat16 bits -> float: the top 16 bits of the f32 pattern. */
+ORC_API float orc_bf16_to_float(uint16_t h) {
+    const uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}

@@ -1,0 +1,124 @@
+"""GPU parity for the prepared AF4-g64 layout: qg_prepare_af4_g64 and
+qmm_af4_g64 (qmm_affine.rs, mlx-native 0.21.1: prepare_af4_g64 and
+dispatch_qmm_affine_t_packed_simd4_b4_gs64_bf16; M <= 32, N and K multiples
+of 64, bf16 scale and bias per 64-group).
+
+The prepared words must equal the oracle's bit for bit. qmm_af4_g64 is held to
+the oracle's qmm_affine on the unprepared codes with the bf16 scales and
+biases taken exactly as f32, under the bar of the kernel that runs: the f32
+bar (1e-5 * sum |x w| + 1e-6) on the CUDA-core path, the tensor-core bar
+(2e-3) where M reaches the tensor-core threshold. Each M at or above that
+threshold is also run with the threshold raised, so both paths meet the
+f32 bar somewhere.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bit_quantized_gemv_dequant_gb300 as qg
+from bit_quantized_gemv_dequant_gb300 import synth
+
+from helpers import assert_bitwise, assert_parity, dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev()).view(
+        torch.bfloat16)
+
+
+def _prepare(c):
+    return qg.prepare_af4_g64(to_dev(c["q"]), _bf16(c["s_bits"]), _bf16(c["b_bits"]))
+
+
+@pytest.fixture
+def min_m():
+    old = qg.get_option(qg.QG_OPT_PREFILL_MIN_M)
+    yield
+    qg.set_option(qg.QG_OPT_PREFILL_MIN_M, old)
+
+
+@pytest.mark.parametrize("N,K", [(64, 64), (192, 512), (128, 4096), (320, 128)])
+def test_prepare_equals_oracle_bitwise(N, K):
+    c = synth.af4_case(7000 + N + K, N, K, 1)
+    plane, meta = _prepare(c)
+    rp, rm = oracle.prepare_af4_g64(c["q"], c["s_bits"], c["b_bits"], N, K)
+    assert_bitwise(plane.cpu().numpy(), rp.view(np.int32), f"af4 plane N={N} K={K}")
+    assert_bitwise(meta.cpu().numpy(), rm.view(np.int32), f"af4 metadata N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 8, 17, 31, 32])
+@pytest.mark.parametrize("N,K", [(64, 64), (192, 512), (128, 1088)])
+def test_qmm_af4_parity(M, N, K, min_m):
+    c = synth.af4_case(7100 + M + N + K, N, K, M)
+    plane, meta = _prepare(c)
+    ref, bound = oracle.qmm_af4_g64(c["x"], c["q"], c["s_bits"], c["b_bits"], M, N, K)
+    tc = M >= qg.get_option(qg.QG_OPT_PREFILL_MIN_M)
+    y = qg.qmm_af4_g64(to_dev(c["x"]), plane, meta, N)
+    assert_parity(y, ref, bound, rel=oracle.REL_TC if tc else oracle.REL,
+                  what=f"qmm_af4_g64 M={M} N={N} K={K}")
+    if tc:
+        qg.set_option(qg.QG_OPT_PREFILL_MIN_M, 64)
+        y = qg.qmm_af4_g64(to_dev(c["x"]), plane, meta, N)
+        assert_parity(y, ref, bound, what=f"qmm_af4_g64 CUDA cores M={M} N={N} K={K}")
+
+
+def test_qmm_af4_page_test_inputs():
+    """The inputs of the page's own bounded-error test (m = 31, n = 64,
+    k = 128: x = 0.5 sin(0.013 i - 0.7), code = (11 i + 3) mod 16, scale
+    bf16(0.01 + 1e-4 i), bias bf16(-0.1 + 2e-4 i)) and its two bounds
+    (relative RMSE and the largest error over max(|y|, 1), each at most
+    5e-3), besides the tensor-core bar."""
+    m, n, k = 31, 64, 128
+    x = (np.sin(np.arange(m * k, dtype=np.float32) * np.float32(0.013) - np.float32(0.7))
+         * np.float32(0.5)).astype(np.float32).reshape(m, k)
+    q = ((np.arange(n * k) * 11 + 3) % 16).astype(np.uint8).reshape(n, k)
+    i = np.arange(n * k // 64, dtype=np.float32)
+    sb = synth.bf16_bits(np.float32(0.01) + i * np.float32(0.0001)).reshape(n, k // 64)
+    bb = synth.bf16_bits(np.float32(-0.1) + i * np.float32(0.0002)).reshape(n, k // 64)
+    plane, meta = qg.prepare_af4_g64(to_dev(q), _bf16(sb), _bf16(bb))
+    y = qg.qmm_af4_g64(to_dev(x), plane, meta, n).cpu().numpy().astype(np.float64)
+    ref, bound = oracle.qmm_af4_g64(x, q, sb, bb, m, n, k)
+    assert_parity(y, ref, bound, rel=oracle.REL_TC, what="qmm_af4_g64 page inputs")
+    err = y - ref
+    assert np.sqrt(np.sum(err * err) / np.sum(ref * ref)) <= 5e-3
+    assert np.max(np.abs(err) / np.maximum(np.abs(ref), 1.0)) <= 5e-3
+
+
+@pytest.mark.parametrize("M", [8, 32])
+def test_qmm_af4_full_size_sampled(M):
+    """The 4096 x 4096 workload the benchmark times, on sampled outputs."""
+    N = K = 4096
+    c = synth.af4_case(7300 + M, N, K, M)
+    plane, meta = _prepare(c)
+    y = qg.qmm_af4_g64(to_dev(c["x"]), plane, meta, N).cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(0, N, 512), np.arange(63, N, 512),
+                                     np.random.default_rng(M).integers(0, N, 32)]))
+    ref, bound = oracle.qmm_af4_g64(c["x"], c["q"], c["s_bits"], c["b_bits"], M, N, K,
+                                    rows=rows)
+    tc = M >= qg.get_option(qg.QG_OPT_PREFILL_MIN_M)
+    assert_parity(y[:, rows], ref[:, rows], bound[:, rows],
+                  rel=oracle.REL_TC if tc else oracle.REL,
+                  what=f"qmm_af4_g64 4096 M={M}")
+
+
+def test_qmm_af4_validation():
+    N, K = 64, 128
+    c = synth.af4_case(7400, N, K, 33)
+    plane, meta = _prepare(c)
+    x = to_dev(c["x"])
+    with pytest.raises(qg.QGError):
+        qg.qmm_af4_g64(x, plane, meta, N)                   # M = 33 > 32
+    with pytest.raises(qg.QGError):
+        qg.qmm_af4_g64(x[:4, :96].contiguous(), plane, meta, N)   # K % 64 != 0
+    with pytest.raises(qg.QGError):
+        qg.qmm_af4_g64(x[:4], plane, meta, 96)              # N % 64 != 0
+    need = qg.workspace_size(qg.QG_OP_AF4_G64, 4, N, K)
+    small = torch.empty(max(need - 256, 0), dtype=torch.uint8, device=dev())
+    with pytest.raises(qg.QGError):
+        qg.qmm_af4_g64(x[:4], plane, meta, N, workspace=small)
+    with pytest.raises(qg.QGError):
+        qg.prepare_af4_g64(to_dev(c["q"][:, :96].copy()), _bf16(c["s_bits"][:, :1].copy()),
+                           _bf16(c["b_bits"][:, :1].copy()))   # K % 64 != 0

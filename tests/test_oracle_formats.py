@@ -142,3 +142,60 @@ def test_qkv_split_concat_is_input_bitwise():
     assert np.array_equal(back.view(np.uint32), bits)
     assert np.array_equal(q.view(np.uint32), bits[:, :qs])
     assert np.array_equal(v.view(np.uint32), bits[:, qs + ks:])
+
+
+def _af4_golden_inputs(N, K):
+    r = np.arange(N)[:, None]
+    k = np.arange(K)[None, :]
+    codes = ((3 * k + k // 16 + r) % 16).astype(np.uint8)
+    h = np.arange(K // 64)[None, :]
+    sb = (0x3C00 + 16 * r + h).astype(np.uint16)
+    bb = (0xBC00 + 16 * r + h).astype(np.uint16)
+    return codes, sb, bb
+
+
+def test_af4_g64_golden_words():
+    fx = _load("af4_g64.json")
+    N, K = fx["N"], fx["K"]
+    codes, sb, bb = _af4_golden_inputs(N, K)
+    plane, meta = oracle.prepare_af4_g64(codes, sb, bb, N, K)
+    assert plane.size == N * K // 8 and meta.size == N * K // 64
+    for item in fx["plane"]:
+        assert plane[item["index"]] == int(item["word"], 16), item
+    for item in fx["metadata"]:
+        assert meta[item["index"]] == int(item["word"], 16), item
+
+
+def test_af4_g64_layout_is_a_permutation():
+    """Every code lands in exactly one nibble: unpacking returns the input, and
+    the plane holds each row's code multiset."""
+    N, K = 192, 256
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    sb = rng.integers(0, 1 << 16, (N, K // 64), dtype=np.uint16)
+    bb = rng.integers(0, 1 << 16, (N, K // 64), dtype=np.uint16)
+    plane, meta = oracle.prepare_af4_g64(codes, sb, bb, N, K)
+    c2, s2, b2 = oracle.af4_unpack(plane, meta, N, K)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, sb) and np.array_equal(b2, bb)
+    # Row 64 + 3 of the plane (second 64-row block) holds only that row's codes.
+    r = 67
+    words = plane.reshape(N // 64, K // 32, 64, 4)[r // 64, :, r % 64, :].ravel()
+    nib = np.concatenate([(words >> (4 * i)) & 15 for i in range(8)])
+    assert np.array_equal(np.bincount(nib, minlength=16), np.bincount(codes[r], minlength=16))
+
+
+def test_af4_bf16_decoder_golden():
+    fx = _load("af4_g64.json")
+    bits = np.array([int(i["bits"], 16) for i in fx["bf16"]], dtype=np.uint16)
+    got = oracle.bf16_to_float_array(bits)
+    for g, item in zip(got, fx["bf16"]):
+        assert float(g) == item["value"], item
+
+
+def test_af4_bf16_decoder_matches_torch():
+    torch = pytest.importorskip("torch")
+    bits = np.arange(0, 1 << 16, 97, dtype=np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # finite values only
+    got = oracle.bf16_to_float_array(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
