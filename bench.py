@@ -250,8 +250,7 @@ def make_single(fmt, M, N, K, case, gs=64, packed=0):
 
 def make_af4(M, N=4096, K=4096, case=90):
     """qmm_af4_g64 on the prepared layout (prepared once, outside the timing):
-    each call unpacks the plane into the packed affine layout, then runs
-    qmm_affine with group size 64."""
+    one kernel reads the prepared words directly."""
     import torch
     import bit_quantized_gemv_dequant_gb300 as qg
     from bit_quantized_gemv_dequant_gb300 import synth
@@ -265,18 +264,16 @@ def make_af4(M, N=4096, K=4096, case=90):
     planes, metas = replicate(plane, ns), replicate(meta, ns)
     xs = replicate(torch.from_numpy(c["x"]).to(dev), ns)
     ys = [torch.empty((M, N), device=dev) for _ in range(ns)]
-    ws = torch.empty(qg.workspace_size(qg.QG_OP_AF4_G64, M, N, K), dtype=torch.uint8,
-                     device=dev)
     L = qg.lib()
 
     def call(i, stream):
         j = i % ns
         rc = L.qmm_af4_g64(xs[j].data_ptr(), planes[j].data_ptr(), metas[j].data_ptr(),
-                           ys[j].data_ptr(), M, N, K, ws.data_ptr(), ws.numel(), stream)
+                           ys[j].data_ptr(), M, N, K, None, 0, stream)
         if rc:
             raise RuntimeError(f"qmm_af4_g64 failed: {qg.status_string(rc)}")
 
-    return Runner(f"af4_g64 M={M} N={N} K={K}", et, 2 * M * N * K, call, ns, 2)
+    return Runner(f"af4_g64 M={M} N={N} K={K}", et, 2 * M * N * K, call, ns, 1)
 
 
 def make_qkv(seq=4096, qs=2048, ks=2048, vs=4096, case=4):
@@ -333,6 +330,7 @@ def sweep_specs():
         ("cfg3 affine u8 M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 0)),
         ("cfg3 affine packed M=512", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 1)),
         ("cfg4 qkv_split", lambda: make_qkv()),
+        ("af4_g64 M=1", lambda: make_af4(1)),
         ("af4_g64 M=8", lambda: make_af4(8)),
         ("af4_g64 M=32", lambda: make_af4(32)),
         # Q4_0 / Q4_K prefill: repacked to affine codes (group 32), tcgen05 MMAs.

@@ -227,7 +227,7 @@ def prepare_af4_g64(codes, scales, biases, *, stream=None):
 
 
 def qmm_af4_g64(x, plane, metadata, N, y=None, *, workspace=None, stream=None):
-    """y[M,N] = x[M,K] . w^T from the prepared AF4-g64 layout (M <= 32)."""
+    """y[M,N] = x[M,K] . w^T from the prepared AF4-g64 layout (M <= 32; no workspace)."""
     M, K = x.shape
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)

@@ -1,6 +1,5 @@
 // The prepared 4-bit affine layout with groups of 64 ("AF4-g64"): the repack
-// tool that writes it, and its unpacking into the packed affine layout that
-// qmm_affine runs on.
+// tool that writes it (this file) and the qmm that reads it (af4_gemv.cu).
 //
 // Page: qmm_affine.rs (mlx-native 0.21.1): prepare_af4_g64 in the test module
 // defines the layout, dispatch_qmm_affine_t_packed_simd4_b4_gs64_bf16 the
@@ -9,8 +8,6 @@
 //    pair p = 0..3 and e0 = 16 (p >> 1) + 4c + 2 (p & 1), code e0 of the
 //    group in bits 4p.. and code e0 + 1 in bits 16 + 4p..;
 //  - metadata u32 [N/64][K/64][64]: bf16 scale | bf16 bias << 16.
-// Each word's pairs are exactly the byte pairs of the packed layout (low
-// nibble = even k), so unpacking is a nibble shuffle.
 #include <algorithm>
 
 #include "qg_internal.cuh"
@@ -58,44 +55,6 @@ __global__ void __launch_bounds__(kThreads) prepare_meta_kernel(const uint16_t* 
     }
 }
 
-// One thread per (row, 32-group): 16 packed code bytes (low nibble = even k)
-// from the group's four plane words; with (row, 64-group) threads writing f32
-// scale and bias (a bf16 value is the f32 with the same top 16 bits).
-__global__ void __launch_bounds__(kThreads) unpack_kernel(const uint32_t* __restrict__ plane,
-                                                           const uint32_t* __restrict__ meta,
-                                                           uint8_t* __restrict__ packed,
-                                                           float* __restrict__ sc,
-                                                           float* __restrict__ bi, int N, int K) {
-    const int G32 = K / 32, G64 = K / 64;
-    const long long total = (long long)N * G32;
-    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
-         t += (long long)gridDim.x * blockDim.x) {
-        const int row = (int)(t / G32), g = (int)(t - (long long)row * G32);
-        const uint4 w4 = *reinterpret_cast<const uint4*>(
-            plane + (((long long)(row / 64) * G32 + g) * 64 + row % 64) * 4);
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-        uint32_t out[4] = {0u, 0u, 0u, 0u};  // 16 bytes: byte i holds k = 2i, 2i + 1
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int e0 = 16 * (p >> 1) + 4 * c + 2 * (p & 1);
-                const uint32_t byte =
-                    ((w[c] >> (4 * p)) & 15u) | (((w[c] >> (16 + 4 * p)) & 15u) << 4);
-                const int bi_ = e0 >> 1;
-                out[bi_ >> 2] |= byte << (8 * (bi_ & 3));
-            }
-        *reinterpret_cast<uint4*>(packed + (long long)row * (K / 2) + g * 16) =
-            make_uint4(out[0], out[1], out[2], out[3]);
-        if ((g & 1) == 0) {
-            const int g64 = g >> 1;
-            const uint32_t m = meta[((long long)(row / 64) * G64 + g64) * 64 + row % 64];
-            sc[(long long)row * G64 + g64] = __uint_as_float(m << 16);
-            bi[(long long)row * G64 + g64] = __uint_as_float(m & 0xFFFF0000u);
-        }
-    }
-}
-
 unsigned blocks_for(const DevCtx& dc, long long total) {
     return (unsigned)std::max<long long>(
         1, std::min<long long>((total + kThreads - 1) / kThreads, (long long)dc.num_sms * 16));
@@ -110,15 +69,6 @@ int af4_prepare_launch(const DevCtx& dc, const uint8_t* codes, const uint16_t* s
                                                                               (int)K);
     prepare_meta_kernel<<<blocks_for(dc, N * (K / 64)), kThreads, 0, s>>>(sb, bb, meta, (int)N,
                                                                          (int)K);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? QG_OK : cuda_fail(e);
-}
-
-int af4_unpack_launch(const DevCtx& dc, const uint32_t* plane, const uint32_t* meta,
-                      uint8_t* packed, float* sc, float* bi, long long N, long long K,
-                      cudaStream_t s) {
-    unpack_kernel<<<blocks_for(dc, N * (K / 32)), kThreads, 0, s>>>(plane, meta, packed, sc, bi,
-                                                                     (int)N, (int)K);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? QG_OK : cuda_fail(e);
 }

@@ -169,33 +169,14 @@ int cuda_fail(cudaError_t e) {
 
 // Workspace bytes of op; with quant_prefill the Q4_0 / Q4_K tensor-core
 // prefill is included.
-// AF4-g64: the unpacked weights (packed codes, f32 scales and biases), then
-// qmm_affine's own workspace.
-struct Af4Layout {
-    size_t sc, bi, rest;
-};
-Af4Layout af4_layout(long long N, long long K) {
-    auto up = [](size_t v) { return (v + 1023) & ~(size_t)1023; };
-    Af4Layout L{};
-    L.sc = up((size_t)N * K / 2);
-    L.bi = L.sc + up((size_t)N * (K / 64) * 4);
-    L.rest = L.bi + up((size_t)N * (K / 64) * 4);
-    return L;
-}
-
 int workspace_size_impl(int op, int64_t M, int64_t N, int64_t K, int group_size, int packed,
                         size_t* bytes, bool quant_prefill) {
     if (!bytes) return QG_ERR_INVALID_ARG;
     *bytes = 0;
-    if (op == QG_OP_AF4_G64) {
+    if (op == QG_OP_AF4_G64) {  // no workspace
         int rc = check_dims(M, N, K);
         if (rc) return rc;
-        if (M > 32 || N % 64 || K % 64) return QG_ERR_INVALID_ARG;
-        size_t inner = 0;
-        rc = workspace_size_impl(QG_OP_AFFINE, M, N, K, 64, 1, &inner, quant_prefill);
-        if (rc) return rc;
-        *bytes = af4_layout(N, K).rest + inner;
-        return QG_OK;
+        return (M > 32 || N % 64 || K % 64) ? QG_ERR_INVALID_ARG : QG_OK;
     }
     GemvArgs a{};
     switch (op) {
@@ -314,29 +295,23 @@ int qg_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales_bf16,
 int qmm_af4_g64(const float* x, const uint32_t* plane, const uint32_t* metadata, float* y,
                 int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                 qg_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
     if (!x || !plane || !metadata || !y) return QG_ERR_INVALID_ARG;
     int rc = check_dims(M, N, K);
     if (rc) return rc;
     if (M > 32 || N % 64 || K % 64) return QG_ERR_INVALID_ARG;
-    if (!aligned(plane, 16) || !aligned(metadata, 4) || (workspace && !aligned(workspace, 16)))
+    if (!aligned(x, 4) || !aligned(y, 4) || !aligned(plane, 16) || !aligned(metadata, 4))
         return QG_ERR_MISALIGNED;
-    size_t need = 0;
-    rc = workspace_size_impl(QG_OP_AF4_G64, M, N, K, 0, 0, &need, true);
-    if (rc) return rc;
-    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE;
+    const long long yb = M * N * 4;
+    if (overlap(y, yb, x, M * K * 4) || overlap(y, yb, plane, N * K / 2) ||
+        overlap(y, yb, metadata, N * (K / 64) * 4))
+        return QG_ERR_INVALID_ARG;
     const DevCtx* dc = nullptr;
     rc = current_ctx(&dc);
     if (rc) return rc;
-    const Af4Layout L = af4_layout(N, K);
-    uint8_t* w8 = static_cast<uint8_t*>(workspace);
-    uint8_t* codes = w8;
-    float* sc = reinterpret_cast<float*>(w8 + L.sc);
-    float* bi = reinterpret_cast<float*>(w8 + L.bi);
-    rc = af4_unpack_launch(*dc, plane, metadata, codes, sc, bi, N, K,
+    return af4_gemv_launch(*dc, x, plane, metadata, y, M, N, K,
                            reinterpret_cast<cudaStream_t>(stream));
-    if (rc) return rc;
-    return qmm_affine(x, codes, sc, bi, y, M, N, K, 64, 1, w8 + L.rest, workspace_bytes - L.rest,
-                      stream);
 }
 
 int qkv_split(const float* qkv, float* q, float* k, float* v, int64_t seq, int64_t q_sp,

@@ -165,14 +165,13 @@ struct GemvArgs {
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a);
 int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
 
-// The prepared AF4-g64 layout (af4.cu): repack from codes and bf16 scale /
-// bias bits, and unpacking into packed affine codes with f32 scales/biases.
+// The prepared AF4-g64 layout: repack from codes and bf16 scale / bias bits
+// (af4.cu), and the qmm that reads it, M <= 32 (af4_gemv.cu).
 int af4_prepare_launch(const DevCtx& dc, const uint8_t* codes, const uint16_t* sb,
                        const uint16_t* bb, uint32_t* plane, uint32_t* meta, long long N,
                        long long K, cudaStream_t s);
-int af4_unpack_launch(const DevCtx& dc, const uint32_t* plane, const uint32_t* meta,
-                      uint8_t* packed, float* sc, float* bi, long long N, long long K,
-                      cudaStream_t s);
+int af4_gemv_launch(const DevCtx& dc, const float* x, const uint32_t* plane, const uint32_t* meta,
+                    float* y, long long M, long long N, long long K, cudaStream_t s);
 
 // Affine prefill on the tensor cores (prefill.cu). Eligibility depends on the
 // shape, the group size, the code and activation pointers' alignment and the

@@ -205,12 +205,12 @@ QG_API int dequant_affine(const void* q, const float* scales, const float* biase
  *
  * qmm_af4_g64: y[M,N] = x[M,K] . w[N,K]^T from the prepared layout, M <= 32
  * (the page's limit). The page's kernel rounds x to bf16 (error class:
- * relative RMS and max |err| / max(|y|, 1) <= 5e-3). Here the prepared layout
- * is unpacked into the workspace as packed affine codes with f32 scales and
- * biases and qmm_affine runs on it, so the result is qmm_affine's: within
- * 1e-5 * sum_k |x w| for M < QG_OPT_PREFILL_MIN_M, 2e-3 * sum_k |x w| on the
- * tensor cores. Needs qg_workspace_size(QG_OP_AF4_G64, M, N, K, 0, 0)
- * bytes. plane, metadata and workspace 16-byte aligned. */
+ * relative RMS and max |err| / max(|y|, 1) <= 5e-3). Here the kernel reads
+ * the prepared words directly and computes in f32 on the CUDA cores for
+ * every M: |y - exact| <= 1e-5 * sum_k |x w| + 1e-6. Row m of y is bitwise
+ * the same whatever M is. x and y 4-byte aligned, plane 16-byte aligned,
+ * metadata 4-byte aligned; y must not overlap an input. No workspace
+ * (qg_workspace_size reports 0; workspace may be NULL). */
 QG_API int qg_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales_bf16,
                               const uint16_t* biases_bf16, uint32_t* plane, uint32_t* metadata,
                               int64_t N, int64_t K, qg_stream_t stream);
