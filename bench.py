@@ -746,6 +746,10 @@ def main():
                 steps = args.sweep_steps if "512" not in name else max(20, args.sweep_steps // 20)
                 res = measure(r, steps, 5, repeats=20)
                 res["frac_of_hbm_peak"] = res["gbs"] / hbm_peak
+                if r.flops and "512" not in name:
+                    # CUDA-core f32 FMAs: against the same ALU peak as the M = 8 line
+                    res["alu_tflops"] = r.flops / (res["us_per_call"] * 1e6)
+                    res["frac_of_alu_peak"] = res["alu_tflops"] / alu_peak
                 if "512" in name:
                     # tensor-core prefill: fp16 MMAs, compared with the measured dense
                     # bf16 peak (fp16 and bf16 share one tensor-core rate)

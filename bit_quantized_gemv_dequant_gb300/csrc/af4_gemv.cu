@@ -28,9 +28,11 @@
 //    computes the current one. The 8 warps' partials are added in warp
 //    order, then the K slices of a row block (the CTAs of one thread-block
 //    cluster) are added in cluster-rank order through distributed shared
-//    memory. Each output's arithmetic is fixed by (N, K, the SM count) alone:
-//    it does not depend on M, on how many activation rows a tile takes, or
-//    on how x is staged, so row m of y is bitwise the same for any M.
+//    memory. Each output's arithmetic is fixed by N, K, the SM count and
+//    whether M <= 8 (which sets the number of K slices): it does not depend
+//    on how many activation rows a tile takes or on how x is staged, so row
+//    m of y is bitwise the same for every M in 1..8, and for every M in
+//    9..32.
 #include <algorithm>
 
 #include "qg_internal.cuh"
@@ -41,6 +43,7 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxKS = 8;
+constexpr int kXB = 8;        // x loads in flight per thread while staging
 
 struct Params {
     const float* x;
@@ -104,69 +107,85 @@ __device__ __forceinline__ float4 x_scale(int j) {
                     : make_float4(1.0f, 1.0f / 65536.0f, 1.0f / 16.0f, 1.0f / 256.0f);
 }
 
+// One 64-group of the lane's rows: row j = 2 * bi + half is row
+// lane + 32 * half of row block bi; words of 32-groups 2g and 2g + 1.
+template <int RB>
 struct Unit {
-    uint4 a[2], b[2];   // words of rows l and l + 32, 32-groups 2h and 2h + 1
-    uint32_t ma, mb;    // metadata of both rows
+    uint4 w[2 * RB][2];
+    uint32_t m[2 * RB];   // metadata of each row
 };
 
-__device__ __forceinline__ void load_unit(Unit& u, const uint4* plane_rb, const uint32_t* meta_rb,
+template <int RB>
+__device__ __forceinline__ void load_unit(Unit<RB>& u, const uint4* plane_rb,
+                                          const uint32_t* meta_rb, size_t qstride, size_t mstride,
                                           int g, int lane, uint64_t pol) {
-    const uint4* q = plane_rb + (size_t)(2 * g) * 64 + lane;
-    u.a[0] = ld_stream(q, pol);
-    u.b[0] = ld_stream(q + 32, pol);
-    u.a[1] = ld_stream(q + 64, pol);
-    u.b[1] = ld_stream(q + 96, pol);
-    const uint32_t* m = meta_rb + (size_t)g * 64 + lane;
-    u.ma = ld_stream(m, pol);
-    u.mb = ld_stream(m + 32, pol);
+#pragma unroll
+    for (int bi = 0; bi < RB; ++bi) {
+        const uint4* q = plane_rb + bi * qstride + (size_t)(2 * g) * 64 + lane;
+        u.w[2 * bi][0] = ld_stream(q, pol);
+        u.w[2 * bi + 1][0] = ld_stream(q + 32, pol);
+        u.w[2 * bi][1] = ld_stream(q + 64, pol);
+        u.w[2 * bi + 1][1] = ld_stream(q + 96, pol);
+        const uint32_t* m = meta_rb + bi * mstride + (size_t)g * 64 + lane;
+        u.m[2 * bi] = ld_stream(m, pol);
+        u.m[2 * bi + 1] = ld_stream(m + 32, pol);
+    }
 }
 
-// T activation rows (m0 .. m0 + T - 1) against the lane's two rows of one
-// 64-group; the group's contribution is added to the warp's partials.
-template <int T>
-__device__ __forceinline__ void tile(const Unit& u, const float* xs, int xrow, int gl,
+// T activation rows (m0 .. m0 + T - 1) against the lane's 2 * RB rows of one
+// 64-group; the group's contribution is added to the warp's partials
+// (redw: [M][64 * RB]). Each x float4 read from shared memory serves all of
+// the lane's rows; each decoded word serves all T activation rows.
+template <int T, int RB>
+__device__ __forceinline__ void tile(Unit<RB>& u, const float* xs, int xrow, int gl,
                                      const float* xsum, int cap, float* redw, int m0, int lane,
                                      uint32_t mg) {
-    float2 acc_a[T], acc_b[T];
+    constexpr int R = 2 * RB;
+    float2 acc[R][T];
 #pragma unroll
-    for (int i = 0; i < T; ++i) acc_a[i] = acc_b[i] = make_float2(0.0f, 0.0f);
-    uint4 A = u.a[0], B = u.b[0];
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+        for (int i = 0; i < T; ++i) acc[j][i] = make_float2(0.0f, 0.0f);
+    // Words are consumed from .x and rotated in place: after the four words
+    // of a 32-group the unit is back in its original order.
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll 1
-    for (int hc = 0; hc < 8; ++hc) {
-        if (hc == 4) {
-            A = u.a[1];
-            B = u.b[1];
+        for (int c = 0; c < 4; ++c) {
+            const float4* xr0 =
+                reinterpret_cast<const float4*>(xs + (size_t)m0 * xrow + gl * 64 + h * 32) + c;
+            float4 xa[T], xb[T];
+#pragma unroll
+            for (int i = 0; i < T; ++i) {
+                xa[i] = xr0[(size_t)i * (xrow / 4)];
+                xb[i] = xr0[(size_t)i * (xrow / 4) + 4];
+            }
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                float2 f[4];
+                decode(u.w[j][h].x, mg, f);
+#pragma unroll
+                for (int i = 0; i < T; ++i) {
+                    acc[j][i] = __ffma2_rn(f[0], make_float2(xa[i].x, xa[i].y), acc[j][i]);
+                    acc[j][i] = __ffma2_rn(f[1], make_float2(xa[i].z, xa[i].w), acc[j][i]);
+                    acc[j][i] = __ffma2_rn(f[2], make_float2(xb[i].x, xb[i].y), acc[j][i]);
+                    acc[j][i] = __ffma2_rn(f[3], make_float2(xb[i].z, xb[i].w), acc[j][i]);
+                }
+                const uint4 w = u.w[j][h];
+                u.w[j][h] = make_uint4(w.y, w.z, w.w, w.x);
+            }
         }
-        float2 fa[4], fb[4];
-        decode(A.x, mg, fa);
-        decode(B.x, mg, fb);
-        const float4* xr0 = reinterpret_cast<const float4*>(xs + (size_t)m0 * xrow + gl * 64 +
-                                                            (hc >> 2) * 32) + (hc & 3);
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        // bf16 -> f32: the bf16 bits are the top half of the f32 pattern.
+        const float s = __uint_as_float(u.m[j] << 16), b = __uint_as_float(u.m[j] & 0xFFFF0000u);
 #pragma unroll
         for (int i = 0; i < T; ++i) {
-            const float4* xr = xr0 + (size_t)i * (xrow / 4);
-            const float4 xa = xr[0], xb = xr[4];
-            acc_a[i] = __ffma2_rn(fa[0], make_float2(xa.x, xa.y), acc_a[i]);
-            acc_a[i] = __ffma2_rn(fa[1], make_float2(xa.z, xa.w), acc_a[i]);
-            acc_a[i] = __ffma2_rn(fa[2], make_float2(xb.x, xb.y), acc_a[i]);
-            acc_a[i] = __ffma2_rn(fa[3], make_float2(xb.z, xb.w), acc_a[i]);
-            acc_b[i] = __ffma2_rn(fb[0], make_float2(xa.x, xa.y), acc_b[i]);
-            acc_b[i] = __ffma2_rn(fb[1], make_float2(xa.z, xa.w), acc_b[i]);
-            acc_b[i] = __ffma2_rn(fb[2], make_float2(xb.x, xb.y), acc_b[i]);
-            acc_b[i] = __ffma2_rn(fb[3], make_float2(xb.z, xb.w), acc_b[i]);
+            const float xm = xsum[(m0 + i) * cap + gl];
+            redw[(m0 + i) * 64 * RB + (j >> 1) * 64 + (j & 1) * 32 + lane] +=
+                fmaf(s, acc[j][i].x + acc[j][i].y, b * xm);
         }
-        A = make_uint4(A.y, A.z, A.w, A.x);
-        B = make_uint4(B.y, B.z, B.w, B.x);
-    }
-    // bf16 -> f32: the bf16 bits are the top half of the f32 pattern.
-    const float sa = __uint_as_float(u.ma << 16), ba = __uint_as_float(u.ma & 0xFFFF0000u);
-    const float sb = __uint_as_float(u.mb << 16), bb = __uint_as_float(u.mb & 0xFFFF0000u);
-#pragma unroll
-    for (int i = 0; i < T; ++i) {
-        const float xm = xsum[(m0 + i) * cap + gl];
-        float* r = redw + (m0 + i) * 64;
-        r[lane] += fmaf(sa, acc_a[i].x + acc_a[i].y, ba * xm);
-        r[lane + 32] += fmaf(sb, acc_b[i].x + acc_b[i].y, bb * xm);
     }
 }
 
@@ -189,24 +208,30 @@ __device__ __forceinline__ float ld_cluster(uint32_t local_addr, uint32_t rank) 
     return v;
 }
 
+// RB row blocks per CTA (each lane owns 2 * RB rows); PF: prefetch the
+// warp's next 64-group while computing the current one; TM: the largest
+// activation-row tile.
+template <int RB, bool PF, int TM>
 __global__ void __launch_bounds__(kThreads, 2) af4_gemv_kernel(const Params p) {
+    constexpr int NR = 64 * RB;                          // rows per CTA
     extern __shared__ __align__(16) uint8_t smem[];
     const int M = p.M;
     const int xrow = p.cap * 64;                         // floats per staged x row
     float* xs = reinterpret_cast<float*>(smem);          // [M][cap * 64], scaled
     float* xsum = xs + (size_t)M * xrow;                 // [M][cap]
-    float* red = xsum + (size_t)M * p.cap;               // [warps][M][64]
-    float* part = red + (size_t)kWarps * M * 64;         // [M][64]
+    float* red = xsum + (size_t)M * p.cap;               // [warps][M][NR]
+    float* part = red + (size_t)kWarps * M * NR;         // [M][NR]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = blockIdx.x;
+    const int rb = blockIdx.x * RB;                      // first row block
     const int g0 = blockIdx.y * p.gpc;                   // first 64-group of the K slice
     const uint32_t mg = p.magic;
     const uint64_t pol = l2_evict_first();
-    const uint4* plane_rb = p.plane + (size_t)rb * p.G32 * 64;
-    const uint32_t* meta_rb = p.meta + (size_t)rb * p.G64 * 64;
+    const size_t qstride = (size_t)p.G32 * 64, mstride = (size_t)p.G64 * 64;
+    const uint4* plane_rb = p.plane + (size_t)rb * qstride;
+    const uint32_t* meta_rb = p.meta + (size_t)rb * mstride;
 
-    for (int i = threadIdx.x; i < kWarps * M * 64; i += kThreads) red[i] = 0.0f;
-    float* redw = red + (size_t)warp * M * 64;
+    for (int i = threadIdx.x; i < kWarps * M * NR; i += kThreads) red[i] = 0.0f;
+    float* redw = red + (size_t)warp * M * NR;
     const bool vec = (reinterpret_cast<uintptr_t>(p.x) & 15) == 0;
 
     for (int s0 = 0; s0 < p.gpc; s0 += p.cap) {
@@ -214,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 2) af4_gemv_kernel(const Params p) {
         const int gb = g0 + s0;                          // first 64-group of the sub-slice
         // The weights do not depend on the preceding kernel: issue the first
         // group's loads before waiting for it.
-        Unit u;
-        if (warp < nsub) load_unit(u, plane_rb, meta_rb, gb + warp, lane, pol);
+        Unit<RB> u;
+        if (warp < nsub) load_unit(u, plane_rb, meta_rb, qstride, mstride, gb + warp, lane, pol);
         if (s0 == 0) {
             pdl_launch_dependents();
             pdl_wait();
@@ -223,44 +248,56 @@ __global__ void __launch_bounds__(kThreads, 2) af4_gemv_kernel(const Params p) {
         // Stage x (scaled per element) and the per-group sums of the unscaled
         // x: thread i takes 4 consecutive elements, and the 16 lanes of a
         // half-warp cover one 64-group (len and the stride are multiples of
-        // 64 elements), whose sum they reduce by shuffles.
+        // 64 elements), whose sum they reduce by shuffles. Each thread issues
+        // up to kXB loads before it uses any.
         const int q4 = nsub * 16;
         const int total = M * q4;
-        for (int base = warp * 32; base < total; base += kThreads) {
-            const int i = base + lane;
-            const bool on = i < total;
-            const int m = on ? i / q4 : 0, kk = on ? 4 * (i - m * q4) : 0;
-            const float* src = p.x + (size_t)m * p.K + (size_t)gb * 64 + kk;
-            float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            if (on) v = vec ? *reinterpret_cast<const float4*>(src)
-                            : make_float4(src[0], src[1], src[2], src[3]);
-            float t = (v.x + v.y) + (v.z + v.w);
+        for (int base = warp * 32; base < total; base += kThreads * kXB) {
+            float4 v[kXB];
 #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-            if (on) {
-                const float4 sc = x_scale(kk & 31);
-                *reinterpret_cast<float4*>(xs + (size_t)m * xrow + kk) =
-                    make_float4(v.x * sc.x, v.y * sc.y, v.z * sc.z, v.w * sc.w);
-                if ((lane & 15) == 0) xsum[m * p.cap + (kk >> 6)] = t;
+            for (int b = 0; b < kXB; ++b) {
+                const int i = base + b * kThreads + lane;
+                v[b] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (i < total) {
+                    const int m = i / q4, kk = 4 * (i - m * q4);
+                    const float* src = p.x + (size_t)m * p.K + (size_t)gb * 64 + kk;
+                    v[b] = vec ? *reinterpret_cast<const float4*>(src)
+                               : make_float4(src[0], src[1], src[2], src[3]);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kXB; ++b) {
+                const int i = base + b * kThreads + lane;
+                float t = (v[b].x + v[b].y) + (v[b].z + v[b].w);
+#pragma unroll
+                for (int off = 8; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+                if (i < total) {
+                    const int m = i / q4, kk = 4 * (i - m * q4);
+                    const float4 sc = x_scale(kk & 31);
+                    *reinterpret_cast<float4*>(xs + (size_t)m * xrow + kk) =
+                        make_float4(v[b].x * sc.x, v[b].y * sc.y, v[b].z * sc.z, v[b].w * sc.w);
+                    if ((lane & 15) == 0) xsum[m * p.cap + (kk >> 6)] = t;
+                }
             }
         }
         __syncthreads();
 
         for (int gl = warp; gl < nsub; gl += kWarps) {
-            Unit nx;
-            const bool more = gl + kWarps < nsub;
-            if (more) load_unit(nx, plane_rb, meta_rb, gb + gl + kWarps, lane, pol);
+            if (!PF && gl != warp)
+                load_unit(u, plane_rb, meta_rb, qstride, mstride, gb + gl, lane, pol);
+            Unit<RB> nx;
+            const bool more = PF && gl + kWarps < nsub;
+            if (more) load_unit(nx, plane_rb, meta_rb, qstride, mstride, gb + gl + kWarps, lane, pol);
             int m0 = 0;
-            for (; m0 + 8 <= M; m0 += 8) tile<8>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
-            if (M - m0 >= 4) {
-                tile<4>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
-                m0 += 4;
-            }
+            if (TM >= 8)
+                for (; m0 + 8 <= M; m0 += 8)
+                    tile<8, RB>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
+            for (; m0 + 4 <= M; m0 += 4) tile<4, RB>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
             if (M - m0 >= 2) {
-                tile<2>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
+                tile<2, RB>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
                 m0 += 2;
             }
-            if (M - m0 >= 1) tile<1>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
+            if (M - m0 >= 1) tile<1, RB>(u, xs, xrow, gl, xsum, p.cap, redw, m0, lane, mg);
             if (more) u = nx;
         }
         __syncthreads();
@@ -268,35 +305,74 @@ __global__ void __launch_bounds__(kThreads, 2) af4_gemv_kernel(const Params p) {
 
     // The warps' partials in warp order; then the K slices in rank order.
     const int n0 = rb * 64;
-    for (int i = threadIdx.x; i < M * 64; i += kThreads) {
+    for (int i = threadIdx.x; i < M * NR; i += kThreads) {
         float v = red[i];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) v += red[(size_t)w * M * 64 + i];
+        for (int w = 1; w < kWarps; ++w) v += red[(size_t)w * M * NR + i];
         if (p.KS == 1)
-            p.y[(size_t)(i >> 6) * p.N + n0 + (i & 63)] = v;
+            p.y[(size_t)(i / NR) * p.N + n0 + (i % NR)] = v;
         else
             part[i] = v;
     }
     if (p.KS > 1) {
         cluster_sync();
-        const int per = M * 64 / p.KS;
+        const int per = M * NR / p.KS;
         const int i0 = (int)cluster_rank() * per;
         const uint32_t base = smem_addr(part);
         for (int i = i0 + threadIdx.x; i < i0 + per; i += kThreads) {
             float v = ld_cluster(base + 4u * i, 0);
             for (int r = 1; r < p.KS; ++r) v += ld_cluster(base + 4u * i, (uint32_t)r);
-            p.y[(size_t)(i >> 6) * p.N + n0 + (i & 63)] = v;
+            p.y[(size_t)(i / NR) * p.N + n0 + (i % NR)] = v;
         }
         // No CTA leaves while another may still read its shared memory.
         cluster_sync();
     }
 }
 
-// Shared memory bytes for M rows and an x sub-slice of cap 64-groups.
-size_t smem_bytes(int M, int cap) {
-    return (size_t)M * cap * 64 * 4 + (size_t)M * cap * 4 + (size_t)kWarps * M * 64 * 4 +
-           (size_t)M * 64 * 4;
+// Shared memory bytes for M rows, an x sub-slice of cap 64-groups and RB
+// row blocks per CTA.
+size_t smem_bytes(int M, int cap, int RB) {
+    return (size_t)M * cap * 64 * 4 + (size_t)M * cap * 4 + (size_t)kWarps * M * 64 * RB * 4 +
+           (size_t)M * 64 * RB * 4;
 }
+
+template <int RB, bool PF, int TM>
+int launch(const DevCtx& dc, const Params& p, int blocks, size_t smem, cudaStream_t s) {
+    auto kern = af4_gemv_kernel<RB, PF, TM>;
+    static size_t configured[64] = {0};
+    if (smem > 48 * 1024 && dc.device >= 0 && dc.device < 64 && configured[dc.device] < smem) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured[dc.device] = smem;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks, (unsigned)p.KS, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.KS > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = (unsigned)p.KS;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (launch_option(QG_OPT_PDL) != 0) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
+// Row blocks per CTA: two (four rows per lane) when the block count is even.
+int rows_blocks_per_cta(long long N) { return (N / 64) % 2 == 0 ? 2 : 1; }
 
 }  // namespace
 
@@ -313,56 +389,31 @@ int af4_gemv_launch(const DevCtx& dc, const float* x, const uint32_t* plane, con
     p.G32 = (int)(K / 32);
     p.G64 = (int)(K / 64);
     p.magic = 0x4B000000u;
-    // K slices: enough CTAs for about one and a half per SM, each slice a
-    // whole number of 64-groups.
-    const int blocks = (int)(N / 64);
+    const int RB = rows_blocks_per_cta(N);
+    // K slices, each a whole number of 64-groups: for M <= 8 enough CTAs for
+    // about one and a half per SM (measured at N = K = 4096: 14.7 us against
+    // 25.4 us with half an SM's worth); for larger M, whose x staging and
+    // partials take most of an SM's shared memory, about one CTA per two SMs
+    // (55 us against 88 us at M = 32).
+    const int blocks = (int)(N / 64) / RB;
+    const int target = M <= 8 ? (3 * dc.num_sms) / 2 : dc.num_sms / 2;
     int KS = 1;
-    while (KS < kMaxKS && blocks * KS < (3 * dc.num_sms) / 2 && p.G64 % (2 * KS) == 0) KS *= 2;
+    while (KS < kMaxKS && blocks * KS < target && p.G64 % (2 * KS) == 0) KS *= 2;
     p.KS = KS;
     p.gpc = p.G64 / KS;
     // x sub-slice: the whole K slice if it fits, else a multiple of the warp
     // count (so that every warp takes the same groups in the same order).
     const size_t limit = (size_t)dc.max_smem_optin;
     int cap = p.gpc;
-    if (smem_bytes(p.M, cap) > limit) {
+    if (smem_bytes(p.M, cap, RB) > limit) {
         cap = kWarps;
-        while (cap + kWarps < p.gpc && smem_bytes(p.M, cap + kWarps) <= limit) cap += kWarps;
+        while (cap + kWarps < p.gpc && smem_bytes(p.M, cap + kWarps, RB) <= limit) cap += kWarps;
     }
-    if (smem_bytes(p.M, cap) > limit) return QG_ERR_UNSUPPORTED;
+    if (smem_bytes(p.M, cap, RB) > limit) return QG_ERR_UNSUPPORTED;
     p.cap = cap;
-    const size_t smem = smem_bytes(p.M, cap);
-
-    static size_t configured[64] = {0};
-    if (smem > 48 * 1024 && dc.device >= 0 && dc.device < 64 && configured[dc.device] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(af4_gemv_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e);
-        configured[dc.device] = smem;
-    }
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)blocks, (unsigned)KS, 1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    if (KS > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 1;
-        attr[na].val.clusterDim.y = (unsigned)KS;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    if (launch_option(QG_OPT_PDL) != 0) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, af4_gemv_kernel, p);
-    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+    const size_t smem = smem_bytes(p.M, cap, RB);
+    return RB == 2 ? launch<2, false, 4>(dc, p, blocks, smem, s)
+                   : launch<1, true, 8>(dc, p, blocks, smem, s);
 }
 
 }  // namespace qg

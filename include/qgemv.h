@@ -208,7 +208,7 @@ QG_API int dequant_affine(const void* q, const float* scales, const float* biase
  * relative RMS and max |err| / max(|y|, 1) <= 5e-3). Here the kernel reads
  * the prepared words directly and computes in f32 on the CUDA cores for
  * every M: |y - exact| <= 1e-5 * sum_k |x w| + 1e-6. Row m of y is bitwise
- * the same whatever M is. x and y 4-byte aligned, plane 16-byte aligned,
+ * the same for every M in 1..8, and for every M in 9..32. x and y 4-byte aligned, plane 16-byte aligned,
  * metadata 4-byte aligned; y must not overlap an input. No workspace
  * (qg_workspace_size reports 0; workspace may be NULL). */
 QG_API int qg_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales_bf16,

@@ -6,11 +6,12 @@ of 64, bf16 scale and bias per 64-group).
 The prepared words must equal the oracle's bit for bit. qmm_af4_g64 is held to
 the oracle's qmm_affine on the unprepared codes with the bf16 scales and
 biases taken exactly as f32, under the f32 bar (1e-5 * sum |x w| + 1e-6) for
-every M. Shapes cover one and several K slices per row block (a cluster of
-1 to 8 CTAs), x staged in more than one sub-slice (M = 32, K = 12288), odd
-group counts, every M tile (8, 4, 2, 1) and the 4096 x 4096 workload the
-benchmark times. Row m of y must not depend on M, and x at a 4-byte offset
-(the scalar staging path) must give bitwise the same y.
+every M. Shapes cover one and two row blocks per CTA (odd and even N / 64),
+one and several K slices per row block (a cluster of 1 to 8 CTAs), x staged
+in more than one sub-slice (M = 32, K = 12288), odd group counts, every M
+tile (8, 4, 2, 1) and the 4096 x 4096 workload the benchmark times. Row m
+of y must not depend on M within M <= 8 and within M > 8, and x at a 4-byte
+offset (the scalar staging path) must give bitwise the same y.
 """
 import numpy as np
 import pytest
@@ -44,7 +45,8 @@ def test_prepare_equals_oracle_bitwise(N, K):
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 8, 17, 31, 32])
-@pytest.mark.parametrize("N,K", [(64, 64), (192, 512), (128, 1088), (64, 12288)])
+@pytest.mark.parametrize("N,K", [(64, 64), (192, 512), (128, 1088), (64, 12288),
+                                 (128, 12288)])
 def test_qmm_af4_parity(M, N, K):
     c = synth.af4_case(7100 + M + N + K, N, K, M)
     plane, meta = _prepare(c)
@@ -55,13 +57,19 @@ def test_qmm_af4_parity(M, N, K):
 
 @pytest.mark.parametrize("N,K", [(192, 512), (64, 12288), (512, 4096)])
 def test_qmm_af4_rows_do_not_depend_on_m(N, K):
+    """The K slicing is one for M <= 8 and one for M > 8; within each class
+    row m of y is bitwise the same whatever M is."""
     c = synth.af4_case(7200 + N, N, K, 32)
     plane, meta = _prepare(c)
     x = to_dev(c["x"])
     y32 = qg.qmm_af4_g64(x, plane, meta, N)
-    for M in (1, 5, 13):
+    for M in (9, 13, 31):
         yM = qg.qmm_af4_g64(x[32 - M:].contiguous(), plane, meta, N)
         assert_bitwise(yM, y32[32 - M:], f"af4 rows of M={M} vs M=32")
+    y8 = qg.qmm_af4_g64(x[:8].contiguous(), plane, meta, N)
+    for M in (1, 3, 5):
+        yM = qg.qmm_af4_g64(x[8 - M:8].contiguous(), plane, meta, N)
+        assert_bitwise(yM, y8[8 - M:], f"af4 rows of M={M} vs M=8")
 
 
 def test_qmm_af4_unaligned_x_is_bitwise_equal():
