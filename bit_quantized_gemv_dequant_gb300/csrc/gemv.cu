@@ -197,6 +197,10 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     const FmtGeo g = geo(a.fmt);
     pl.MT = Mc <= 1 ? 1 : Mc <= 2 ? 2 : Mc <= 4 ? 4 : 8;
     pl.W = pl.MT <= 2 ? 16 : 12;
+    // Q4_K with M bucket 8: eight consumer warps, one CTA per SM, so that a
+    // stage can hold two rows (each x chunk then serves two rows).
+    const bool q4k8 = a.fmt == FMT_Q4_K && pl.MT == 8;
+    if (q4k8) pl.W = 8;
     // Eight consumer warps (two CTAs per SM: this launch's and the next one's)
     // when requested; M = 1 only.
     const bool w8 = pl.MT == 1 && launch_option(QG_OPT_STAGED_WARPS) == 8;
@@ -240,11 +244,12 @@ Plan make_plan(const DevCtx& dc, const GemvArgs& a, int Mc) {
     long long best_key = -1;
     for (int ri = 0; ri < nr; ++ri) {
         const int R = ropt[ri];
-        if (R > fast::max_rows(a.fmt, pl.MT)) continue;
+        if (R > fast::max_rows(a.fmt, pl.MT, pl.W)) continue;
         if (w8 && R < 4) continue;
         const int V = pl.MT * R;
         const int sums = g.sums ? pl.MT * pl.P * 32 * g.nh : 0;
         for (int co = 1; co >= (w8 ? 1 : 0); --co) {
+            if (co && q4k8) continue;  // its registers allow one CTA per SM
             const int stage = ((R * pl.q_stride + 2 * R * pl.sb_stride + 16) + 127) & ~127;
             const int budget = co ? co_budget : dc.max_smem_optin;
             // Per stage: the copy, two mbarriers, an arrival counter and the

@@ -274,8 +274,11 @@ __device__ __forceinline__ void butterfly(float (&v)[V], int lane) {
     }
 }
 
+// Eight consumer warps with M bucket 1 leave room for two CTAs per SM (this
+// launch's and the next one's); with larger M buckets they run one CTA per SM
+// and up to 168 registers a thread (three warps per SM sub-partition).
 template <int FMT, int MT, int R, int W, int GW>
-__global__ void __launch_bounds__((W + 1) * 32, W == 8 ? 2 : 1) gemv_fast_kernel(const Params p) {
+__global__ void __launch_bounds__((W + 1) * 32, (W == 8 && MT == 1) ? 2 : 1) gemv_fast_kernel(const Params p) {
     using F = Fmt<FMT>;
     constexpr int UE = F::UE;
     constexpr int NCH = UE / 4;       // float4 chunks of x per unit
@@ -734,12 +737,15 @@ int launch(const DevCtx& dc, const Params& kp, int grid_x, int smem, bool pdl, c
 namespace qg {
 namespace fast {
 
-// Largest rows-per-stage per (format, M bucket) that compiles without
-// register spills (16 consumer warps + producer cap a thread at 96
-// registers; 12 + producer, used for M >= 4, at 128).
-__host__ __device__ constexpr int max_rows(int fmt, int MT) {
+// Largest rows-per-stage per (format, M bucket, consumer warps) that compiles
+// without register spills. An SM sub-partition holds 16 K registers, so the
+// warps it runs share them: 16 consumer warps + producer (five on one
+// sub-partition) cap a thread at 96 registers, 12 + producer (four) at 128,
+// and 8 + producer (three) at 168 when one CTA runs per SM. Q4_K with M
+// bucket 8 runs 8 consumer warps to take two rows per stage.
+__host__ __device__ constexpr int max_rows(int fmt, int MT, int W) {
     return fmt == FMT_Q4_0   ? (MT == 1 ? 16 : MT == 8 ? 2 : 4)
-           : fmt == FMT_Q4_K ? (MT == 1 ? 4 : MT == 8 ? 1 : 2)
+           : fmt == FMT_Q4_K ? (MT == 1 ? 4 : MT == 8 ? (W == 8 ? 2 : 1) : 2)
                              : (MT == 1 ? 16 : 2);
 }
 
@@ -748,7 +754,7 @@ __host__ __device__ constexpr int max_rows(int fmt, int MT) {
 template <int FMT, int MT, int W, int R>
 int dispatch_gw(const DevCtx& dc, const Params& kp, int GW, int grid, int smem, bool pdl,
                 cudaStream_t s) {
-    if constexpr (R > max_rows(FMT, MT)) {
+    if constexpr (R > max_rows(FMT, MT, W)) {
         return QG_ERR_UNSUPPORTED;
     } else {
         switch (GW) {
@@ -782,6 +788,12 @@ int dispatch(const DevCtx& dc, const Params& kp, int MT, int R, int GW, int W, i
             if (R <= 2) return dispatch_gw<FMT, 4, 12, 2>(dc, kp, GW, grid, smem, pdl, s);
             return dispatch_gw<FMT, 4, 12, 4>(dc, kp, GW, grid, smem, pdl, s);
         default:
+            if constexpr (FMT == FMT_Q4_K) {
+                if (W == 8) {
+                    if (R <= 1) return dispatch_gw<FMT, 8, 8, 1>(dc, kp, GW, grid, smem, pdl, s);
+                    return dispatch_gw<FMT, 8, 8, 2>(dc, kp, GW, grid, smem, pdl, s);
+                }
+            }
             if (R <= 1) return dispatch_gw<FMT, 8, 12, 1>(dc, kp, GW, grid, smem, pdl, s);
             if (R == 2) return dispatch_gw<FMT, 8, 12, 2>(dc, kp, GW, grid, smem, pdl, s);
             return dispatch_gw<FMT, 8, 12, 4>(dc, kp, GW, grid, smem, pdl, s);
