@@ -738,9 +738,7 @@ namespace qg {
 namespace fast {
 
 // Largest rows-per-stage per (format, M bucket, consumer warps) that compiles
-// without register spills (one exception: Q4_K with M bucket 8 and 2 rows
-// spills a few dozen bytes, and is still faster than 1 row with 12 warps).
-// An SM sub-partition holds 16 K registers, so the
+// without register spills. An SM sub-partition holds 16 K registers, so the
 // warps it runs share them: 16 consumer warps + producer (five on one
 // sub-partition) cap a thread at 96 registers, 12 + producer (four) at 128,
 // and 8 + producer (three) at 168 when one CTA runs per SM. Q4_K with M
