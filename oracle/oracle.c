@@ -317,10 +317,19 @@ ORC_API void orc_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales,
                 uint32_t word = 0;
                 for (int p = 0; p < 4; ++p) {
                     const int64_t e = g * 32 + 16 * (p / 2) + 4 * c + 2 * (p % 2);
+#ifdef ORACLE_PLANT_AF4_HALVES
+                    word |= (uint32_t)(codes[r * K + e + 1] & 15u) << (4 * p);
+                    word |= (uint32_t)(codes[r * K + e] & 15u) << (16 + 4 * p);
+#else
                     word |= (uint32_t)(codes[r * K + e] & 15u) << (4 * p);
                     word |= (uint32_t)(codes[r * K + e + 1] & 15u) << (16 + 4 * p);
+#endif
                 }
+#ifdef ORACLE_PLANT_AF4_ROW_MAJOR
+                plane[(r * g32n + g) * 4 + c] = word;
+#else
                 plane[(((r / 64) * g32n + g) * 64 + r % 64) * 4 + c] = word;
+#endif
             }
     }
 }

@@ -73,6 +73,25 @@ def test_validation_needs_no_gpu(lib):
     k = lib.qgemv_q4_k
     k.argtypes = [P, P, P, I64, I64, I64, P, C.c_size_t, P]
     assert k(fake, fake + 4096, fake + 8192, 1, 4, 128, None, 0, None) == 1  # K % 256
+    a = lib.qmm_af4_g64
+    a.argtypes = [P, P, P, P, I64, I64, I64, P, C.c_size_t, P]
+    x, pl, me, y = fake, fake + 65536, fake + 131072, fake + 196608
+    assert a(x, pl, me, y, 33, 64, 64, None, 0, None) == 1      # M > 32
+    assert a(x, pl, me, y, 1, 96, 64, None, 0, None) == 1       # N % 64
+    assert a(x, pl, me, y, 1, 64, 96, None, 0, None) == 1       # K % 64
+    assert a(None, pl, me, y, 1, 64, 64, None, 0, None) == 1
+    assert a(x, pl + 4, me, y, 1, 64, 64, None, 0, None) == 3   # plane not 16-byte aligned
+    assert a(x, pl, me, x, 1, 64, 64, None, 0, None) == 1       # y overlaps x
+    pr = lib.qg_prepare_af4_g64
+    pr.argtypes = [P, P, P, P, P, I64, I64, P]
+    assert pr(fake, fake + 8192, fake + 12288, pl, me, 64, 96, None) == 1   # K % 64
+    assert pr(fake, fake + 8192, fake + 12288, pl + 8, me, 64, 64, None) == 3
+    assert pr(fake, None, fake + 12288, pl, me, 64, 64, None) == 1
+    ws = C.c_size_t(7)
+    lib.qg_workspace_size.argtypes = [C.c_int, I64, I64, I64, C.c_int, C.c_int,
+                                      C.POINTER(C.c_size_t)]
+    assert lib.qg_workspace_size(4, 32, 64, 128, 0, 0, C.byref(ws)) == 0 and ws.value == 0
+    assert lib.qg_workspace_size(4, 33, 64, 128, 0, 0, C.byref(ws)) == 1
 
 
 def test_launch_options_round_trip_and_validation(lib):
