@@ -23,8 +23,10 @@
  *    there interoperates with the GGUF Q4K type, whose field layout is the
  *    reading taken below.
  *  - qmm_affine.rs (mlx-native 0.21.1), test module: the CPU reference
- *    qmm_affine_t_cpu (w = q*s + b per group along K, f64 accumulation) and
- *    pack_b4_to_u32 (code j of a u32 word sits at bits 4j).
+ *    qmm_affine_t_cpu (w = q*s + b per group along K, f64 accumulation),
+ *    pack_b4_to_u32 (code j of a u32 word sits at bits 4j) and
+ *    prepare_af4_g64 (the prepared layout with 64-groups and bf16 scale and
+ *    bias bits, written out below as orc_prepare_af4_g64).
  *  - qkv_split.rs (mlx-native 0.7.1), module doc: per token the fused row is
  *    [Q | K | V]; every element goes to exactly one output.
  *
