@@ -166,10 +166,10 @@ def test_af4_g64_golden_words():
         assert meta[item["index"]] == int(item["word"], 16), item
 
 
-def test_af4_g64_layout_is_a_permutation():
+@pytest.mark.parametrize("N,K", [(192, 256), (64, 64), (320, 1088), (128, 4096)])
+def test_af4_g64_layout_is_a_permutation(N, K):
     """Every code lands in exactly one nibble: unpacking returns the input, and
     the plane holds each row's code multiset."""
-    N, K = 192, 256
     rng = np.random.default_rng(5)
     codes = rng.integers(0, 16, (N, K), dtype=np.uint8)
     sb = rng.integers(0, 1 << 16, (N, K // 64), dtype=np.uint16)
@@ -177,8 +177,8 @@ def test_af4_g64_layout_is_a_permutation():
     plane, meta = oracle.prepare_af4_g64(codes, sb, bb, N, K)
     c2, s2, b2 = oracle.af4_unpack(plane, meta, N, K)
     assert np.array_equal(c2, codes) and np.array_equal(s2, sb) and np.array_equal(b2, bb)
-    # Row 64 + 3 of the plane (second 64-row block) holds only that row's codes.
-    r = 67
+    # The last row's words (the last 64-row block) hold only that row's codes.
+    r = N - 1
     words = plane.reshape(N // 64, K // 32, 64, 4)[r // 64, :, r % 64, :].ravel()
     nib = np.concatenate([(words >> (4 * i)) & 15 for i in range(8)])
     assert np.array_equal(np.bincount(nib, minlength=16), np.bincount(codes[r], minlength=16))
