@@ -8,7 +8,9 @@ loaded on first use, and every call raises if it has not been built or no
 CUDA device is present: there is no CPU fallback.
 
 Workspace: calls that need device scratch (split-K partial sums) get it from
-a per-device torch buffer that grows on demand, unless the caller passes one.
+a torch buffer per (device, stream) that grows on demand, unless the caller
+passes one. Calls on different streams therefore never share scratch; calls
+on one stream are ordered by the stream.
 """
 from __future__ import annotations
 
@@ -127,17 +129,20 @@ def workspace_size(op: int, M: int, N: int, K: int, group_size: int = 0, packed:
     return int(n.value)
 
 
-def _workspace(op, M, N, K, gs, packed, device, workspace):
+def _workspace(op, M, N, K, gs, packed, device, workspace, stream):
     need = workspace_size(op, M, N, K, gs, packed)
     if workspace is not None:
         return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     if need == 0:
         return None, 0
-    key = torch.device(device).index
-    buf = _WS.get(key)
-    if buf is None or buf.numel() < need:
-        buf = torch.empty(need, dtype=torch.uint8, device=device)
-        _WS[key] = buf
+    # One buffer per (device, stream): two calls on different streams may run
+    # at the same time and must not share split-K scratch.
+    key = (torch.device(device).index, stream)
+    with _LOCK:
+        buf = _WS.get(key)
+        if buf is None or buf.numel() < need:
+            buf = torch.empty(need, dtype=torch.uint8, device=device)
+            _WS[key] = buf
     return buf.data_ptr(), buf.numel()
 
 
@@ -148,9 +153,10 @@ def qgemv_q4_0(w, x, y=None, *, N=None, workspace=None, stream=None):
     N = N if N is not None else w.numel() // (K // 32 * 18)
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    ws, wsb = _workspace(QG_OP_Q4_0, M, N, K, 0, 0, x.device, workspace)
+    st = _stream(stream)
+    ws, wsb = _workspace(QG_OP_Q4_0, M, N, K, 0, 0, x.device, workspace, st)
     _check(lib().qgemv_q4_0(_dev(w, "w", torch.uint8), _dev(x, "x", torch.float32),
-                            _dev(y, "y", torch.float32), M, N, K, ws, wsb, _stream(stream)),
+                            _dev(y, "y", torch.float32), M, N, K, ws, wsb, st),
            "qgemv_q4_0")
     return y
 
@@ -163,11 +169,12 @@ def qgemv_dual_q4_0(w_a, w_b, x, y_a=None, y_b=None, *, N=None, workspace=None, 
         y_a = torch.empty((M, N), dtype=torch.float32, device=x.device)
     if y_b is None:
         y_b = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    ws, wsb = _workspace(QG_OP_DUAL_Q4_0, M, N, K, 0, 0, x.device, workspace)
+    st = _stream(stream)
+    ws, wsb = _workspace(QG_OP_DUAL_Q4_0, M, N, K, 0, 0, x.device, workspace, st)
     _check(lib().qgemv_dual_q4_0(_dev(w_a, "w_a", torch.uint8), _dev(w_b, "w_b", torch.uint8),
                                  _dev(x, "x", torch.float32), _dev(y_a, "y_a", torch.float32),
                                  _dev(y_b, "y_b", torch.float32), M, N, K, ws, wsb,
-                                 _stream(stream)), "qgemv_dual_q4_0")
+                                 st), "qgemv_dual_q4_0")
     return y_a, y_b
 
 
@@ -177,9 +184,10 @@ def qgemv_q4_k(w, x, y=None, *, N=None, workspace=None, stream=None):
     N = N if N is not None else w.numel() // (K // 256 * 144)
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    ws, wsb = _workspace(QG_OP_Q4_K, M, N, K, 0, 0, x.device, workspace)
+    st = _stream(stream)
+    ws, wsb = _workspace(QG_OP_Q4_K, M, N, K, 0, 0, x.device, workspace, st)
     _check(lib().qgemv_q4_k(_dev(w, "w", torch.uint8), _dev(x, "x", torch.float32),
-                            _dev(y, "y", torch.float32), M, N, K, ws, wsb, _stream(stream)),
+                            _dev(y, "y", torch.float32), M, N, K, ws, wsb, st),
            "qgemv_q4_k")
     return y
 
@@ -203,11 +211,12 @@ def qmm_affine(x, q, scales, biases, group_size, packed, y=None, *, workspace=No
     N = scales.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    ws, wsb = _workspace(QG_OP_AFFINE, M, N, K, group_size, int(packed), x.device, workspace)
+    st = _stream(stream)
+    ws, wsb = _workspace(QG_OP_AFFINE, M, N, K, group_size, int(packed), x.device, workspace, st)
     _check(lib().qmm_affine(_dev(x, "x", torch.float32), _dev(q, "q", torch.uint8),
                             _dev(scales, "scales", torch.float32),
                             _dev(biases, "biases", torch.float32), _dev(y, "y", torch.float32),
-                            M, N, K, int(group_size), int(packed), ws, wsb, _stream(stream)),
+                            M, N, K, int(group_size), int(packed), ws, wsb, st),
            "qmm_affine")
     return y
 
@@ -231,10 +240,11 @@ def qmm_af4_g64(x, plane, metadata, N, y=None, *, workspace=None, stream=None):
     M, K = x.shape
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    ws, wsb = _workspace(QG_OP_AF4_G64, M, N, K, 0, 0, x.device, workspace)
+    st = _stream(stream)
+    ws, wsb = _workspace(QG_OP_AF4_G64, M, N, K, 0, 0, x.device, workspace, st)
     _check(lib().qmm_af4_g64(_dev(x, "x", torch.float32), _dev(plane, "plane", torch.int32),
                              _dev(metadata, "metadata", torch.int32), _dev(y, "y", torch.float32),
-                             M, N, K, ws, wsb, _stream(stream)), "qmm_af4_g64")
+                             M, N, K, ws, wsb, st), "qmm_af4_g64")
     return y
 
 

@@ -21,26 +21,26 @@ constexpr size_t kNoAllocScratchBytes = 4u << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDev = 64;
-std::once_flag g_once[kMaxDev];
-void* g_addr[kMaxDev];
-int g_rc[kMaxDev];
+std::mutex g_lock;
+void* g_addr[kMaxDev];  // non-null once the lookup has succeeded on that device
 
 // Device address of the scratch array on the current device. The host-side
 // name g_noalloc_scratch is only a stand-in for the symbol; the address a
-// kernel may use comes from cudaGetSymbolAddress, taken once per device with
-// that device current.
+// kernel may use comes from cudaGetSymbolAddress, taken with that device
+// current. Only a successful lookup is kept: a failed one (for example a
+// first call made inside a stream capture) is retried by the next call.
 int scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDev) return QG_ERR_UNSUPPORTED;
-    std::call_once(g_once[dev], [dev] {
+    std::lock_guard<std::mutex> lk(g_lock);
+    if (!g_addr[dev]) {
         void* p = nullptr;
-        const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_rc[dev] = (err == cudaSuccess) ? QG_OK : cuda_fail(err);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
         g_addr[dev] = p;
-    });
-    if (g_rc[dev] != QG_OK) return g_rc[dev];
+    }
     *out = g_addr[dev];
     return QG_OK;
 }
@@ -58,6 +58,8 @@ extern "C" int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64
     rc = qg::scratch_address(&scratch);
     if (rc != QG_OK) return rc;
     // The split-K partial sums are fully written before they are read, so
-    // nothing in the scratch array needs clearing between calls.
-    return qgemv_q4_k(w, x, y, M, N, K, scratch, qg::kNoAllocScratchBytes, stream);
+    // nothing in the scratch array needs clearing between calls. The call
+    // stays on the CUDA-core kernels for every M: the tensor-core prefill
+    // would need scratch for rewritten weights, and has a looser error bound.
+    return qg::q4_k_cuda_core(w, x, y, M, N, K, scratch, qg::kNoAllocScratchBytes, stream);
 }

@@ -148,6 +148,25 @@ int run_gemv(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
 
 }  // namespace
 
+int q4_k_cuda_core(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
+                   void* ws, size_t ws_bytes, qg_stream_t stream) {
+    GemvArgs a{};
+    a.fmt = FMT_Q4_K;
+    a.nw = 1;
+    a.w[0] = static_cast<const uint8_t*>(w);
+    a.y[0] = y;
+    a.x = x;
+    a.M = M; a.N = N; a.K = K;
+    int rc = validate_gemv(a);
+    if (rc) return rc;
+    if (ws && !aligned(ws, 16)) return QG_ERR_MISALIGNED;
+    const DevCtx* dc = nullptr;
+    rc = current_ctx(&dc);
+    if (rc) return rc;
+    if (gemv_workspace_bytes(*dc, a) > (ws ? ws_bytes : 0)) return QG_ERR_WORKSPACE;
+    return gemv_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
 long long launch_option(int option) {
     switch (option) {
         case QG_OPT_PDL: return g_opt_pdl.load(std::memory_order_relaxed);

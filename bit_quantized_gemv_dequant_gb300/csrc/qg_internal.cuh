@@ -195,6 +195,11 @@ int dequant_launch(const DevCtx& dc, int fmt, const uint8_t* w, const float* sca
                    cudaStream_t s);
 int selftest_wait_launch(const DevCtx& dc, long long timeout_ns, cudaStream_t s);
 
+// qgemv_q4_k restricted to its CUDA-core kernels (never the tensor-core
+// prefill, whatever M and the workspace): same validation, same status codes.
+int q4_k_cuda_core(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
+                   void* ws, size_t ws_bytes, qg_stream_t stream);
+
 // Workspace of the CUDA-core path alone (qg_workspace_size also covers the
 // Q4_0 / Q4_K tensor-core prefill, which calls with a smaller workspace skip).
 int cuda_core_workspace_size(int op, int64_t M, int64_t N, int64_t K, size_t* bytes);

@@ -135,16 +135,18 @@ QG_API int qgemv_q4_k(const void* w, const float* x, float* y, int64_t M, int64_
  * and accuracy as qgemv_q4_k, but the split-K scratch that qgemv_q4_k takes
  * as a workspace comes from a 4 MiB array in the library's own device memory
  * (held on every GPU that loads the library until the process exits).
- * - Returns QG_ERR_WORKSPACE, before enqueuing anything, when the shape needs
- *   more than 4 MiB of scratch (qg_workspace_size(QG_OP_Q4_K, ...) > 4 MiB).
+ * - Returns QG_ERR_WORKSPACE, before enqueuing anything, when the CUDA-core
+ *   kernels need more than 4 MiB of split-K scratch for the shape (at most
+ *   qg_workspace_size(QG_OP_Q4_K, ...), which also covers the prefill).
  * - Allocates nothing. The first call on a device looks up the array's device
  *   address (cudaGetSymbolAddress); make that first call before any stream
- *   capture.
+ *   capture. A failed lookup is not remembered: the next call tries again.
  * - All calls share the one array: calls that may overlap on the GPU (other
  *   streams, other host threads) race on it. Its contents are fully rewritten
  *   before they are read, so nothing needs clearing between calls.
- * - Always takes qgemv_q4_k's CUDA-core path: the tensor-core prefill needs a
- *   workspace for the rewritten weights, which this entry point does not have. */
+ * - Always takes qgemv_q4_k's CUDA-core kernels, for every M, with their f32
+ *   bound (1e-5 * sum_k |x w| + 1e-6): the tensor-core prefill needs scratch
+ *   for the rewritten weights, which this entry point does not have. */
 QG_API int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M, int64_t N,
                               int64_t K, qg_stream_t stream);
 

@@ -303,7 +303,7 @@ ORC_API void orc_qkv_split(const uint32_t* qkv, uint32_t* q, uint32_t* k, uint32
 /*   code[r][e] in bits 4p.. and code[r][e + 1] in bits 16 + 4p..;           */
 /*   meta[((r / 64) * K/64 + h) * 64 + r % 64] = scale bits | bias bits << 16 */
 /*   for the 64-wide group h.                                                */
-/* Parity pins: a hand-computed word (tests/golden/af4_g64.txt) and the      */
+/* Parity pins: a hand-computed word (tests/golden/af4_g64.json) and the     */
 /* round trip through orc_af4_unpack.                                        */
 /* ------------------------------------------------------------------------ */
 ORC_API void orc_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales,

@@ -6,8 +6,6 @@ Collected last on purpose: a run that stops at the first failure has run
 every other test before this one. It also passes on its own in a fresh
 process: it builds all its inputs itself and needs no state from other tests.
 """
-import ctypes as C
-
 import numpy as np
 import pytest
 import torch
@@ -43,13 +41,39 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
     assert qg.device_error() == 0
 
 
+@pytest.mark.parametrize("M", [16, 24, 32])
+@pytest.mark.parametrize("N", [64, 256])
+def test_noalloc_stays_on_cuda_cores_for_large_m(M, N):
+    # From M = 16 up, qgemv_q4_k with a large enough workspace may take the
+    # tensor-core prefill (error bound 2e-3 * sum |x w|). The no-alloc entry
+    # point must keep the CUDA-core kernels and their f32 bound for every M,
+    # whatever the size of its scratch array. x is 16-byte aligned here, which
+    # the prefill also asks for.
+    K = 4096
+    qg.set_option(qg.QG_OPT_PREFILL_MIN_M, 16)
+    c = synth.q4_k_case(3100 + M + N, N, K, M)
+    w, x = to_dev(c["w"]), to_dev(c["x"])
+    assert x.data_ptr() % 16 == 0
+    for call in range(2):
+        y = qg.qgemv_q4_k_noalloc(w, x, N=N)
+        torch.cuda.synchronize()
+        ref, bound = oracle.gemv_q4_k(c["w"], c["x"], M, N, K)
+        assert_parity(y, ref, bound, what=f"no-alloc M={M} N={N} call {call}")
+    assert qg.device_error() == 0
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     # 3 slices x 8 rows x 65536 outputs x 4 bytes = 6 MiB > 4 MiB: refused with
-    # QG_ERR_WORKSPACE before anything is enqueued (the pointers are never used).
+    # QG_ERR_WORKSPACE before anything is enqueued. The buffers are real and
+    # sized for the shape, so that a regression in the size check would run a
+    # kernel on valid memory and show up as a wrong return code.
     M, N, K = 8, 65536, 12288
     assert qg.workspace_size(qg.QG_OP_Q4_K, M, N, K) > (4 << 20)
-    fake = 1 << 20
-    rc = qg.lib().qgemv_q4_k_noalloc(C.c_void_p(fake), C.c_void_p(fake + (1 << 12)),
-                                     C.c_void_p(fake + (1 << 13)), M, N, K,
+    w = torch.zeros(N * (K // 256) * 144, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.float32, device="cuda")
+    y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    rc = qg.lib().qgemv_q4_k_noalloc(w.data_ptr(), x.data_ptr(), y.data_ptr(), M, N, K,
                                      torch.cuda.current_stream().cuda_stream)
     assert rc == qg.QG_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert not y.any()
