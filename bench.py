@@ -40,7 +40,6 @@ L2_BYTES = 129 * 1024 * 1024
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-SM_COUNT_NOMINAL = 152
 
 
 def peaks():
@@ -383,6 +382,13 @@ def time_runner(r: Runner, steps: int, warmup: int, chunk: int = 1000):
     return graphs, stream
 
 
+# A bounded sleep kernel (fixed cycle count, no flag) queued ahead of the start
+# event: the host enqueues the graphs while it runs, so the timed region starts
+# with the work already queued and measures the calls, not the host's graph
+# launch latency (which matters for short runs such as 20 steps).
+QUEUE_AHEAD_US = 100.0
+
+
 def replay_timed(graphs, stream, barrier=None):
     import torch
     e0 = torch.cuda.Event(enable_timing=True)
@@ -392,6 +398,7 @@ def replay_timed(graphs, stream, barrier=None):
     torch.cuda.synchronize()
     t0 = time.time()
     with torch.cuda.stream(stream):  # replay() launches on the current stream
+        torch.cuda._sleep(int(QUEUE_AHEAD_US * 2.1e3))  # ~100 us at up to 2.1 GHz
         e0.record(stream)
         for g in graphs:
             g.replay()
@@ -417,38 +424,70 @@ def measure(r: Runner, steps: int, warmup: int, repeats: int = 1):
 
 
 # --------------------------------------------------------------- e2e
-def e2e_dual(r: Runner, steps: int, warmup: int):
-    """Same workload through the public C ABI with host buffers: every step
-    copies x from pinned host memory, runs the dual projection and reads
-    y_a, y_b back into pinned host memory, then waits for them."""
+def e2e_dual(steps: int, warmup: int, M: int = 1, N: int = 4096, K: int = 4096):
+    """The headline workload end to end, through the public C ABI with host
+    buffers: every step copies x from pinned host memory to the device, runs
+    the dual projection, copies y_a and y_b (one [2, M, N] buffer) back into
+    pinned host memory and waits for them on the host. The three operations of
+    a step are one CUDA graph (two cudaMemcpyAsync and one call), replayed
+    once per step. Also reported: the same loop with the copies left out and
+    with the call left out (the host round trip and the copies alone)."""
     import torch
-    H = r.host
-    M, N, K = H["M"], H["N"], H["K"]
-    x_host = torch.from_numpy(H["c"]["x"]).pin_memory()
-    ya_h = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    yb_h = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    import bit_quantized_gemv_dequant_gb300 as qg
+    from bit_quantized_gemv_dequant_gb300 import synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    c = synth.q4_0_case(1, N, K, M, dual=True)
+    wa, wb = torch.from_numpy(c["w"]).to(dev), torch.from_numpy(c["w_b"]).to(dev)
+    x_host = torch.from_numpy(c["x"]).pin_memory()
+    y_host = torch.empty((2, M, N), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((M, K), device=dev)
+    y_dev = torch.empty((2, M, N), device=dev)
+    L = qg.lib()
     stream = torch.cuda.Stream()
-    ns = r.nsets
 
-    def step(i):
-        j = i % ns
+    def graph(copies, call):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            h = stream.cuda_stream
+            if copies:
+                x_dev.copy_(x_host, non_blocking=True)
+            if call:
+                rc = L.qgemv_dual_q4_0(wa.data_ptr(), wb.data_ptr(), x_dev.data_ptr(),
+                                       y_dev[0].data_ptr(), y_dev[1].data_ptr(), M, N, K,
+                                       None, 0, h)
+                if rc:
+                    raise RuntimeError(f"qgemv_dual_q4_0 failed: {qg.status_string(rc)}")
+            if copies:
+                y_host.copy_(y_dev, non_blocking=True)
+        return g
+
+    def run(g, n):
+        for _ in range(n):
+            g.replay()
+            stream.synchronize()
+
+    out = {}
+    for name, copies, call in (("full", True, True), ("call_only", False, True),
+                               ("copies_only", True, False)):
+        g = graph(copies, call)
         with torch.cuda.stream(stream):
-            H["xs"][j].copy_(x_host, non_blocking=True)
-            r.call(i, stream.cuda_stream)
-            ya_h.copy_(H["ya"][j], non_blocking=True)
-            yb_h.copy_(H["yb"][j], non_blocking=True)
-        stream.synchronize()
-
-    for i in range(warmup):
-        step(i)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(steps):
-        step(i)
-    t1 = time.perf_counter()
-    us = 1e6 * (t1 - t0) / steps
-    return {"value": r.et_bytes / (us * 1e3), "unit": "GB/s", "us_per_step": us,
-            "h2d_bytes_per_step": 4 * M * K, "d2h_bytes_per_step": 2 * 4 * M * N}
+            run(g, warmup)
+            t0 = time.perf_counter()
+            run(g, steps)
+            t1 = time.perf_counter()
+        out[name] = 1e6 * (t1 - t0) / steps
+        del g
+    if not np.isfinite(y_host.numpy()).all():
+        raise RuntimeError("e2e: non-finite output copied back")
+    et = 2 * N * q4_0_row_bytes(K) + 4 * M * K + 2 * 4 * M * N
+    us = out["full"]
+    return {"value": et / (us * 1e3), "unit": "GB/s", "us_per_step": us,
+            "h2d_bytes_per_step": 4 * M * K, "d2h_bytes_per_step": 2 * 4 * M * N,
+            "breakdown_us": {"step (copies + call + host wait)": out["full"],
+                             "call + host wait, no copies": out["call_only"],
+                             "copies + host wait, no call": out["copies_only"]},
+            "how": "one CUDA graph per step (H2D copy of x, the dual call, one D2H copy of "
+                   "y_a and y_b), replayed and waited for on the host every step"}
 
 
 # -------------------------------------------------------------- traffic
@@ -604,8 +643,9 @@ def main():
     ap.add_argument("--only", default=None, metavar="NAME",
                     help="time one sweep configuration (e.g. 'cfg3 affine u8 M=512') for "
                          "--steps calls and print its line; for profiling runs")
-    ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
-                    help="launch with programmatic dependent launch (weights are static)")
+    ap.add_argument("--pdl", type=int, default=2, choices=[0, 1, 2],
+                    help="QG_OPT_PDL for the headline: 2 = independent back-to-back calls "
+                         "(default), 1 = each call waits for the previous one, 0 = plain launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -690,14 +730,25 @@ def main():
                         "traffic": recorded_traffic("gemv_q4_0_dual_m1")},
            "clocks": clocks}
 
-    out["launch_mode"] = ("CUDA graph of back-to-back calls" +
-                          (", programmatic dependent launch (QG_OPT_PDL: static weights)"
-                           if args.pdl else ""))
-    if args.pdl:
-        # The same workload without programmatic dependent launch, for reference.
-        qg.set_option(qg.QG_OPT_PDL, 0)
-        out["no_pdl"] = measure(r1, min(args.steps, 20000), args.warmup)
-        qg.set_option(qg.QG_OPT_PDL, 1)
+    out["launch_mode"] = {
+        2: "CUDA graph of back-to-back independent calls (QG_OPT_PDL = 2: each call reads "
+           "and writes only its own buffers, so consecutive calls overlap)",
+        1: "CUDA graph of back-to-back calls, each waiting for the previous one "
+           "(QG_OPT_PDL = 1, programmatic dependent launch)",
+        0: "CUDA graph of back-to-back calls, plain launches"}[args.pdl]
+    out["queue_ahead"] = (f"graphs queued behind a {QUEUE_AHEAD_US:.0f} us sleep kernel before "
+                          "the start event")
+    # The same workload in the other launch modes, for reference: a chain in
+    # which every call waits for the previous one (a decode chain whose x is
+    # the previous y), and plain launches.
+    for mode, key in ((1, "dependent_chain"), (0, "no_pdl")):
+        if mode == args.pdl:
+            continue
+        qg.set_option(qg.QG_OPT_PDL, mode)
+        res = measure(r1, min(args.steps, 20000), args.warmup)
+        res["frac_of_hbm_peak"] = res["gbs"] / hbm_peak
+        out[key] = res
+    qg.set_option(qg.QG_OPT_PDL, args.pdl)
 
     # Hot L2 (labelled as such, not the headline): one weight set reused by
     # every call, so the 18.9 MB of weights stay in the 129 MB L2.
@@ -711,15 +762,16 @@ def main():
     r8 = make_dual_q4_0(8)
     m8 = measure(r8, min(args.steps, 20000), args.warmup)
     sm_mhz = clocks.get("sm_max_mhz") or peak_doc.get("sm_max_mhz") or 2070.0
-    alu_peak = SM_COUNT_NOMINAL * 128 * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s f32 FMA
+    n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    alu_peak = n_sm * 128 * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s f32 FMA
     tflops = r8.flops / (m8["us_per_call"] * 1e-6) / 1e12
     m8.update({"frac_of_hbm_peak": m8["gbs"] / hbm_peak,
                "roofline": {"bound": "alu", "achieved": tflops, "peak": alu_peak,
                             "unit": "TFLOP/s", "frac": tflops / alu_peak,
-                            "peak_source": "152 SMs x 128 f32 FMA/clk x 2 x max SM clock"}})
+                            "peak_source": f"{n_sm} SMs x 128 f32 FMA/clk x 2 x max SM clock"}})
     out["m8"] = m8
 
-    out["e2e"] = e2e_dual(r1, min(2000, max(50, args.steps // 100)), 20)
+    out["e2e"] = e2e_dual(min(2000, max(200, args.steps // 100)), 20)
 
     if not args.no_cpu:
         gbs1, rows1, calls1, dt1 = oracle_dual_sample(1, 4096, 4096, budget_s=6.0)
@@ -746,6 +798,15 @@ def main():
                 steps = args.sweep_steps if "512" not in name else max(20, args.sweep_steps // 20)
                 res = measure(r, steps, 5, repeats=20)
                 res["frac_of_hbm_peak"] = res["gbs"] / hbm_peak
+                if "decode layer" in name and args.pdl != 1:
+                    # The same four projections when each waits for the one
+                    # before it (a decode chain whose inputs are outputs).
+                    qg.set_option(qg.QG_OPT_PDL, 1)
+                    dep = measure(r, steps, 5, repeats=20)
+                    qg.set_option(qg.QG_OPT_PDL, args.pdl)
+                    res["dependent_chain"] = {"us_per_call": dep["us_per_call"],
+                                              "gbs": dep["gbs"],
+                                              "frac_of_hbm_peak": dep["gbs"] / hbm_peak}
                 if r.flops and "512" not in name:
                     # CUDA-core f32 FMAs: against the same ALU peak as the M = 8 line
                     res["alu_tflops"] = r.flops / (res["us_per_call"] * 1e6)

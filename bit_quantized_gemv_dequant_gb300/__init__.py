@@ -32,6 +32,10 @@ QG_OPT_STREAM, QG_OPT_STREAM_WARPS, QG_OPT_STREAM_SLOTS = 3, 4, 5
 QG_OPT_STAGES_AHEAD = 6
 QG_OPT_STAGED_WARPS = 7
 QG_OPT_PREFILL_FOLD = 8
+QG_OPT_XREG = 9
+QG_OPT_XREG_AHEAD = 10
+QG_OPT_XREG_WARPS = 11
+QG_OPT_XREG_CTAS = 12
 
 EXPORTS = ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_split",
            "dequant_q4_0", "dequant_q4_k", "dequant_affine", "qg_workspace_size",

@@ -17,6 +17,7 @@
 
 #include "gemv_fast.cuh"
 #include "gemv_stream.cuh"
+#include "gemv_xreg.cuh"
 #include "qg_internal.cuh"
 
 namespace qg {
@@ -382,6 +383,94 @@ SPlan make_stream_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float*
     return sp;
 }
 
+// ------------------------------------------------------------ xreg plan
+// The register-resident-x kernel (gemv_xreg.cuh) for Mc <= 2. Its geometry
+// (warps per row group, consumer warps, rows per chunk) depends on the format
+// and K only, never on N or the number of matrices.
+struct XPlan {
+    bool ok;
+    int NWC, WG, NRG, RC, S, slot_bytes, sb_off, smem, grid, units, rbuf, red_floats;
+};
+
+XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x) {
+    XPlan xp{};
+    xp.ok = false;
+    if (Mc > 2 || launch_option(QG_OPT_XREG) == 0) return xp;
+    const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
+    if (a.K % 32 || a.K > 16384) return xp;
+    const long long units = a.K / 32;
+    long long WG;
+    if (a.fmt == FMT_Q4_0) {
+        if (a.K % 256) return xp;          // 16-byte aligned rows
+        WG = 2 * ((units + 63) / 64);      // warps of one block parity each
+    } else {
+        if (affine && (a.gs < 32 || (a.K / a.gs) % 4)) return xp;
+        WG = (units + 31) / 32;
+    }
+    if (WG > 16) return xp;
+    for (int i = 0; i < a.nw; ++i)
+        if (!aligned16(a.w[i])) return xp;
+    if (!aligned16(x)) return xp;
+    if (affine && (!aligned16(a.scales) || !aligned16(a.biases))) return xp;
+    if ((long long)a.nw * a.N >= (1ll << 31)) return xp;
+    int NWC = (8 % WG == 0) ? 8 : (12 % WG == 0) ? 12 : 16;
+    // Four consumer warps (four CTAs, i.e. four calls, per SM) when calls are
+    // declared independent (QG_OPT_PDL = 2): consecutive calls then overlap,
+    // and more of them in flight hide each CTA's start-up and tail. A call
+    // that waits for its predecessor computes alone, and does better with
+    // eight warps (two CTAs per SM: this call's and the next one's).
+    const long long want_w = launch_option(QG_OPT_XREG_WARPS);
+    if (WG <= 4 && 4 % WG == 0 &&
+        (want_w == 4 || (want_w == 0 && launch_option(QG_OPT_PDL) == 2)))
+        NWC = 4;
+    if (NWC == 16 && Mc == 2) return xp;  // two x rows need more registers than 17 warps allow
+    const int NRG = std::min<int>(8, NWC / (int)WG);
+    const int RC = NRG * xreg::kRPG;
+    const long long rb = row_bytes(a.fmt, a.K);
+    const int G = affine ? (int)(a.K / a.gs) : 0;
+    const long long slot = ((RC * rb + (affine ? 2ll * RC * G * 4 : 0)) + 127) & ~127ll;
+    // Packed and one-code-per-byte affine calls must take the same kernel
+    // (their results are bitwise equal only then): whether the plan fits is
+    // decided on the larger, one-code-per-byte slot for both.
+    const long long slot_fit = affine ? ((RC * a.K + 2ll * RC * G * 4) + 127) & ~127ll : slot;
+    // Rows of per-warp partial sums buffered before a flush: the CTA's whole
+    // share when it fits in 16 KB, and never fewer than one chunk.
+    const long long ctas_per_sm = std::max<long long>(1, launch_option(QG_OPT_XREG_CTAS));
+    const long long grid_max = (long long)dc.num_sms * ctas_per_sm;
+    const long long rows_cta = ((long long)a.nw * a.N + grid_max - 1) / grid_max;
+    const long long rbuf = std::max<long long>(RC, std::min<long long>(rows_cta, 4096 / (Mc * WG)));
+    const long long per_slot = slot + 16;
+    // Partial sums, then the staging area of x (Mc * K floats).
+    const long long red_floats = (rbuf * Mc * WG + 3) & ~3ll;
+    const long long fixed = (red_floats + (long long)Mc * a.K) * 4 + (long long)NWC * Mc * 4 + 128;
+    // Eight consumer warps with one input row fit twice on an SM (this call's
+    // CTA and the next one's); otherwise one CTA per SM.
+    // Four consumer warps: four CTAs per SM.
+    const bool co = (NWC == 8 && Mc == 1) || NWC == 4;
+    const int per_sm = NWC == 4 ? 4 : 2;
+    long long budget = co ? (long long)dc.smem_per_sm / per_sm - dc.reserved_smem : dc.max_smem_optin;
+    long long S = std::min<long long>(16, (budget - fixed) / per_slot);
+    if ((budget - fixed) / (slot_fit + 16) < 2) {
+        budget = dc.max_smem_optin;
+        S = std::min<long long>(16, (budget - fixed) / per_slot);
+    }
+    if ((budget - fixed) / (slot_fit + 16) < 2) return xp;
+    xp.NWC = NWC;
+    xp.WG = (int)WG;
+    xp.NRG = NRG;
+    xp.RC = RC;
+    xp.S = (int)S;
+    xp.slot_bytes = (int)slot;
+    xp.sb_off = (int)(RC * rb);
+    xp.smem = (int)(S * per_slot + fixed - 128);
+    xp.grid = (int)std::min<long long>((long long)a.nw * a.N, grid_max);
+    xp.units = (int)units;
+    xp.rbuf = (int)rbuf;
+    xp.red_floats = (int)red_floats;
+    xp.ok = true;
+    return xp;
+}
+
 template <int FMT>
 int launch_general(const DevCtx& dc, const KParams& kp, cudaStream_t s) {
     const long long rows = (long long)kp.nw * kp.N;
@@ -399,6 +488,11 @@ int stream_launch_aff_u8(const DevCtx&, const stream::Params&, int, int, int, in
                          cudaStream_t);
 int stream_launch_aff_packed(const DevCtx&, const stream::Params&, int, int, int, int, int, bool,
                              cudaStream_t);
+int xreg_launch_q4_0(const DevCtx&, const xreg::Params&, int, int, int, int, bool, cudaStream_t);
+int xreg_launch_q4_k(const DevCtx&, const xreg::Params&, int, int, int, int, bool, cudaStream_t);
+int xreg_launch_aff_u8(const DevCtx&, const xreg::Params&, int, int, int, int, bool, cudaStream_t);
+int xreg_launch_aff_packed(const DevCtx&, const xreg::Params&, int, int, int, int, bool,
+                           cudaStream_t);
 int fast_launch_q4_0(const DevCtx&, const fast::Params&, int, int, int, int, int, int, bool,
                       cudaStream_t);
 int fast_launch_q4_k(const DevCtx&, const fast::Params&, int, int, int, int, int, int, bool,
@@ -427,6 +521,57 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
         float* y0 = a.y[0] + m0 * a.N;
         float* y1 = (a.nw > 1 ? a.y[1] : a.y[0]) + m0 * a.N;
         int rc;
+        const XPlan xp = make_xreg_plan(dc, a, Mc, x);
+        if (xp.ok) {
+            xreg::Params kp{};
+            kp.w[0] = a.w[0];
+            kp.w[1] = a.nw > 1 ? a.w[1] : a.w[0];
+            kp.out[0] = y0;
+            kp.out[1] = y1;
+            kp.x = x;
+            kp.s = a.scales;
+            kp.b = a.biases;
+            kp.M = Mc;
+            kp.N = (int)a.N;
+            kp.K = (int)a.K;
+            kp.nw = a.nw;
+            kp.log2gs = affine ? ilog2(a.gs) : 0;
+            kp.G = affine ? (int)(a.K / a.gs) : 0;
+            kp.row_bytes = (int)row_bytes(a.fmt, a.K);
+            const int rows_total = (int)(a.nw * a.N);
+            kp.rows_base = rows_total / xp.grid;
+            kp.rows_rem = rows_total % xp.grid;
+            kp.S = xp.S;
+            kp.slot_bytes = xp.slot_bytes;
+            kp.sb_off = xp.sb_off;
+            kp.WG = xp.WG;
+            kp.NRG = xp.NRG;
+            kp.RC = xp.RC;
+            kp.units = xp.units;
+            kp.rbuf = xp.rbuf;
+            kp.red_floats = xp.red_floats;
+            kp.ahead = (int)std::min<long long>(launch_option(QG_OPT_XREG_AHEAD), xp.S);
+            kp.err = dc.err;
+            const long long pdl_mode = launch_option(QG_OPT_PDL);
+            const bool pdl = pdl_mode != 0;
+            kp.dep_wait = pdl_mode == 2 ? 0 : 1;
+            switch (a.fmt) {
+                case FMT_Q4_0:
+                    rc = xreg_launch_q4_0(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    break;
+                case FMT_Q4_K:
+                    rc = xreg_launch_q4_k(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    break;
+                case FMT_AFF_U8:
+                    rc = xreg_launch_aff_u8(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    break;
+                default:
+                    rc = xreg_launch_aff_packed(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    break;
+            }
+            if (rc != QG_OK) return rc;
+            continue;
+        }
         const SPlan sp = make_stream_plan(dc, a, Mc, x);
         if (sp.ok) {
             stream::Params kp{};

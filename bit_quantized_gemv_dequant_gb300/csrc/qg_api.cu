@@ -30,6 +30,10 @@ std::atomic<long long> g_opt_stream_slots{0};
 std::atomic<long long> g_opt_ahead{2};
 std::atomic<long long> g_opt_staged_warps{0};
 std::atomic<long long> g_opt_prefill_fold{0};
+std::atomic<long long> g_opt_xreg{1};
+std::atomic<long long> g_opt_xreg_ahead{0};
+std::atomic<long long> g_opt_xreg_warps{0};
+std::atomic<long long> g_opt_xreg_ctas{1};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -177,6 +181,10 @@ long long launch_option(int option) {
         case QG_OPT_STAGES_AHEAD: return g_opt_ahead.load(std::memory_order_relaxed);
         case QG_OPT_STAGED_WARPS: return g_opt_staged_warps.load(std::memory_order_relaxed);
         case QG_OPT_PREFILL_FOLD: return g_opt_prefill_fold.load(std::memory_order_relaxed);
+        case QG_OPT_XREG: return g_opt_xreg.load(std::memory_order_relaxed);
+        case QG_OPT_XREG_AHEAD: return g_opt_xreg_ahead.load(std::memory_order_relaxed);
+        case QG_OPT_XREG_WARPS: return g_opt_xreg_warps.load(std::memory_order_relaxed);
+        case QG_OPT_XREG_CTAS: return g_opt_xreg_ctas.load(std::memory_order_relaxed);
         default: return 0;
     }
 }
@@ -404,7 +412,7 @@ int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_size, i
 int qg_set_option(int option, int64_t value) {
     switch (option) {
         case QG_OPT_PDL:
-            if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
+            if (value < 0 || value > 2) return QG_ERR_INVALID_ARG;
             g_opt_pdl.store(value, std::memory_order_relaxed);
             return QG_OK;
         case QG_OPT_PREFILL_MIN_M:
@@ -435,6 +443,22 @@ int qg_set_option(int option, int64_t value) {
             if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
             g_opt_prefill_fold.store(value, std::memory_order_relaxed);
             return QG_OK;
+        case QG_OPT_XREG:
+            if (value != 0 && value != 1) return QG_ERR_INVALID_ARG;
+            g_opt_xreg.store(value, std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_XREG_AHEAD:
+            if (value < 0 || value > 16) return QG_ERR_INVALID_ARG;
+            g_opt_xreg_ahead.store(value, std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_XREG_WARPS:
+            if (value != 0 && value != 4) return QG_ERR_INVALID_ARG;
+            g_opt_xreg_warps.store(value, std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_XREG_CTAS:
+            if (value < 1 || value > 4) return QG_ERR_INVALID_ARG;
+            g_opt_xreg_ctas.store(value, std::memory_order_relaxed);
+            return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }
 }
@@ -459,6 +483,16 @@ int qg_get_option(int option, int64_t* value) {
             return QG_OK;
         case QG_OPT_PREFILL_FOLD:
             *value = g_opt_prefill_fold.load(std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_XREG: *value = g_opt_xreg.load(std::memory_order_relaxed); return QG_OK;
+        case QG_OPT_XREG_AHEAD:
+            *value = g_opt_xreg_ahead.load(std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_XREG_WARPS:
+            *value = g_opt_xreg_warps.load(std::memory_order_relaxed);
+            return QG_OK;
+        case QG_OPT_XREG_CTAS:
+            *value = g_opt_xreg_ctas.load(std::memory_order_relaxed);
             return QG_OK;
         default: return QG_ERR_INVALID_ARG;
     }

@@ -235,7 +235,16 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * caller promises that the weight codes, scales and biases of a call are not
  * written by the kernel immediately preceding it on the stream (static model
  * weights satisfy this). Back-to-back decode projections overlap one call's
- * ramp-up with the previous call's tail this way. */
+ * ramp-up with the previous call's tail this way.
+ *
+ * QG_OPT_PDL = 2 adds a second promise: the call reads nothing the kernel
+ * immediately preceding it on the stream writes, and writes nothing that
+ * kernel reads or writes (independent projections, e.g. several projections
+ * of one input, or calls on distinct buffers). The register-resident-x
+ * kernel (QG_OPT_XREG) then does not wait for its predecessor at all, so
+ * consecutive independent calls run concurrently, two CTAs per SM; the other
+ * kernels behave as with 1. A kernel launched after such a call without
+ * programmatic dependent launch still waits for it as usual. */
 /*
  * QG_OPT_PREFILL_MIN_M (default 16, >= 1): smallest M for which qmm_affine
  * takes the tensor-core prefill path (when its other conditions hold). */
@@ -275,9 +284,27 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * accumulator over all of K, faster. Both stay within 2e-3 * sum_k |x w|
  * for weight rows whose scales span less than 2^29; 0 keeps the weights
  * exact whatever their spread. */
+/*
+ * QG_OPT_XREG (default 1; or 0): calls with M <= 2 (per slice of x) take the
+ * register-resident-x kernel when it is eligible: K % 32 == 0, K <= 16384,
+ * Q4_0 rows 16-byte aligned (K % 256 == 0), affine group size >= 32 with
+ * (K / group_size) % 4 == 0, and the weight, x (and affine scale / bias)
+ * pointers 16-byte aligned. 0 leaves those calls to the other CUDA-core
+ * kernels. Like QG_OPT_STREAM, the choice never depends on N or on single
+ * versus dual calls.
+ *
+ * QG_OPT_XREG_AHEAD (default 0 = every slot of the ring; else 1..16): chunks
+ * of weights the register-resident-x kernel keeps in flight at most (tuning).
+ *
+ * QG_OPT_XREG_WARPS (default 0 = automatic; or 4) and QG_OPT_XREG_CTAS
+ * (default 1; 1..4): consumer warps per CTA and CTAs per SM per call of the
+ * register-resident-x kernel (tuning; results are bitwise the same). With
+ * four consumer warps (rows of at most 4096 weights of K), four CTAs share an
+ * SM; automatic picks them when QG_OPT_PDL is 2, eight warps otherwise. */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
        QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6, QG_OPT_STAGED_WARPS = 7,
-       QG_OPT_PREFILL_FOLD = 8 };
+       QG_OPT_PREFILL_FOLD = 8, QG_OPT_XREG = 9, QG_OPT_XREG_AHEAD = 10,
+       QG_OPT_XREG_WARPS = 11, QG_OPT_XREG_CTAS = 12 };
 QG_API int qg_set_option(int option, int64_t value);
 QG_API int qg_get_option(int option, int64_t* value);
 

@@ -100,14 +100,18 @@ def test_launch_options_round_trip_and_validation(lib):
     lib.qg_set_option.argtypes = [C.c_int, C.c_int64]
     lib.qg_get_option.argtypes = [C.c_int, C.POINTER(C.c_int64)]
     get = lambda o: (lambda v: (lib.qg_get_option(o, C.byref(v)), v.value))(C.c_int64())
-    cases = {1: ([0, 1], [2, -1]),            # QG_OPT_PDL
+    cases = {1: ([0, 1, 2], [3, -1]),         # QG_OPT_PDL
              2: ([1, 64], [0]),               # QG_OPT_PREFILL_MIN_M
              3: ([0, 1, 2], [3, -1]),         # QG_OPT_STREAM
              4: ([0, 1, 8], [9, -1]),         # QG_OPT_STREAM_WARPS
              5: ([0, 2, 8], [1, 9]),          # QG_OPT_STREAM_SLOTS
              6: ([0, 1, 64], [65, -1]),       # QG_OPT_STAGES_AHEAD
              7: ([0, 8], [4, 16]),            # QG_OPT_STAGED_WARPS
-             8: ([0, 1], [2, -1])}            # QG_OPT_PREFILL_FOLD
+             8: ([0, 1], [2, -1]),            # QG_OPT_PREFILL_FOLD
+             9: ([0, 1], [2, -1]),            # QG_OPT_XREG
+             10: ([0, 1, 16], [17, -1]),      # QG_OPT_XREG_AHEAD
+             11: ([4, 0], [8, -1]),           # QG_OPT_XREG_WARPS
+             12: ([2, 4, 1], [0, 5])}         # QG_OPT_XREG_CTAS
     for opt, (good, bad) in cases.items():
         rc, old = get(opt)
         assert rc == 0

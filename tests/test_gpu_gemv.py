@@ -276,8 +276,16 @@ def test_no_device_error_left():
     assert qg.device_error() == 0
 
 
+@pytest.fixture
+def staged_m1():
+    """M = 1 calls on the staged kernel (the register-resident-x kernel off)."""
+    qg.set_option(qg.QG_OPT_XREG, 0)
+    yield
+    qg.set_option(qg.QG_OPT_XREG, 1)
+
+
 @pytest.mark.parametrize("ahead", [0, 1, 3])
-def test_stages_ahead_does_not_change_results(ahead):
+def test_stages_ahead_does_not_change_results(ahead, staged_m1):
     """QG_OPT_STAGES_AHEAD only changes when chunks are requested, never the
     arithmetic: results are bitwise equal to the default schedule."""
     M, N, K = 1, 700, 4096
@@ -294,7 +302,7 @@ def test_stages_ahead_does_not_change_results(ahead):
     assert_bitwise(yb, base[1], f"ahead={ahead} y_b")
 
 
-def test_eight_warp_coresident_variant_is_bitwise_equal():
+def test_eight_warp_coresident_variant_is_bitwise_equal(staged_m1):
     """QG_OPT_STAGED_WARPS = 8 changes the CTA shape (and lets the next launch's
     CTA share the SM), never an output's arithmetic."""
     M, N, K = 1, 900, 4096

@@ -23,10 +23,13 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(autouse=True)
 def stream_opts():
-    """Every eligible call takes the streaming kernel here; the options are
-    restored afterwards."""
+    """Every eligible call takes the streaming kernel here (the register-resident-x
+    kernel, which would take most of them first, is switched off); the options
+    are restored afterwards."""
     qg.set_option(qg.QG_OPT_STREAM, 2)
+    qg.set_option(qg.QG_OPT_XREG, 0)
     yield
+    qg.set_option(qg.QG_OPT_XREG, 1)
     qg.set_option(qg.QG_OPT_STREAM, 1)
     qg.set_option(qg.QG_OPT_STREAM_WARPS, 0)
     qg.set_option(qg.QG_OPT_STREAM_SLOTS, 0)

@@ -1,0 +1,282 @@
+"""GPU parity of the register-resident-x GEMV kernel (calls with M <= 2).
+
+Same tolerance as every f32 GEMV test, per output:
+|y - ref| <= 1e-5 * sum_k |x_k w_k| + 1e-6 against the oracle's f64 reference.
+Covered: every format, M = 1 and 2, K from 256 to 16384 (one to sixteen warps
+per row group, Q4_0 blocks of both parities, partly filled warps), ragged row
+counts and chunks that straddle the two matrices of a dual call, the full
+workload sizes, the dual projection bitwise equal to two single ones, packed
+affine codes bitwise equal to one code per byte, an exact integer closed form,
+activations spanning the f32 exponent range (the kernel scales x by one power
+of two chosen from max|x|), non-finite x, and agreement with the older
+CUDA-core kernels (QG_OPT_XREG = 0).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import bit_quantized_gemv_dequant_gb300 as qg
+from bit_quantized_gemv_dequant_gb300 import synth
+
+from helpers import assert_bitwise, assert_parity, to_dev
+
+pytestmark = pytest.mark.gpu
+
+Q4_0_SHAPES = [(37, 256), (61, 1024), (45, 2048), (70, 3072), (300, 4096), (19, 8192),
+               (23, 12288), (9, 16384)]
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K", Q4_0_SHAPES)
+def test_xreg_q4_0_dual_and_single(M, N, K):
+    c = synth.q4_0_case(5000 + 7 * M + N, N, K, M, dual=True)
+    wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
+    ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    sa = qg.qgemv_q4_0(wa, x, N=N)
+    sb = qg.qgemv_q4_0(wb, x, N=N)
+    assert_bitwise(ya, sa, f"dual vs single y_a M={M} N={N} K={K}")
+    assert_bitwise(yb, sb, f"dual vs single y_b M={M} N={N} K={K}")
+    (ra, ba), (rb, bb) = oracle.gemv_dual_q4_0(c["w"], c["w_b"], c["x"], M, N, K)
+    assert_parity(ya, ra, ba, what=f"q4_0 y_a M={M} N={N} K={K}")
+    assert_parity(yb, rb, bb, what=f"q4_0 y_b M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K", [(29, 256), (50, 1024), (33, 3072), (64, 4096), (21, 8192),
+                                 (17, 12288), (11, 16384)])
+def test_xreg_q4_k(M, N, K):
+    c = synth.q4_k_case(5100 + M + N, N, K, M)
+    y = qg.qgemv_q4_k(to_dev(c["w"]), to_dev(c["x"]), N=N)
+    ref, bound = oracle.gemv_q4_k(c["w"], c["x"], M, N, K)
+    assert_parity(y, ref, bound, what=f"q4_k M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K,gs", [(37, 1024, 32), (64, 4096, 64), (20, 2048, 128),
+                                    (17, 4096, 256), (25, 8192, 512), (16, 4096, 1024),
+                                    (13, 12288, 64)])
+def test_xreg_affine_packed_equals_u8(M, N, K, gs):
+    c = synth.affine_case(5200 + M + N + gs, N, K, M, gs)
+    x, s, b = to_dev(c["x"]), to_dev(c["s"]), to_dev(c["b"])
+    yu = qg.qmm_affine(x, to_dev(c["q"]), s, b, gs, 0)
+    yp = qg.qmm_affine(x, to_dev(c["q_packed"]), s, b, gs, 1)
+    assert_bitwise(yp, yu, f"packed vs u8 M={M} N={N} K={K} gs={gs}")
+    ref, bound = oracle.qmm_affine(c["x"], c["q"], c["s"], c["b"], M, N, K, gs, False)
+    assert_parity(yu, ref, bound, what=f"affine M={M} N={N} K={K} gs={gs}")
+
+
+def test_xreg_full_workloads():
+    """The benchmark's M = 1 shapes at full size: config 0, config 1 (dual),
+    config 2 (Q4_K N = 4096 and 12288, and the FFN down shape) and config 3."""
+    c = synth.q4_0_case(0, 1024, 1024, 1)
+    y = qg.qgemv_q4_0(to_dev(c["w"]), to_dev(c["x"]), N=1024)
+    assert_parity(y, *oracle.gemv_q4_0(c["w"], c["x"], 1, 1024, 1024), what="config 0")
+    c = synth.q4_0_case(1, 4096, 4096, 1, dual=True)
+    ya, yb = qg.qgemv_dual_q4_0(to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"]), N=4096)
+    (ra, ba), (rb, bb) = oracle.gemv_dual_q4_0(c["w"], c["w_b"], c["x"], 1, 4096, 4096)
+    assert_parity(ya, ra, ba, what="config 1 y_a")
+    assert_parity(yb, rb, bb, what="config 1 y_b")
+    for N, K in ((4096, 4096), (12288, 4096), (4096, 12288)):
+        c = synth.q4_k_case(2, N, K, 1)
+        y = qg.qgemv_q4_k(to_dev(c["w"]), to_dev(c["x"]), N=N)
+        assert_parity(y, *oracle.gemv_q4_k(c["w"], c["x"], 1, N, K), what=f"q4_k N={N} K={K}")
+    c = synth.affine_case(3, 4096, 4096, 1, 64)
+    for packed in (0, 1):
+        q = c["q_packed"] if packed else c["q"]
+        y = qg.qmm_affine(to_dev(c["x"]), to_dev(q), to_dev(c["s"]), to_dev(c["b"]), 64, packed)
+        ref, bound = oracle.qmm_affine(c["x"], c["q"], c["s"], c["b"], 1, 4096, 4096, 64, False)
+        assert_parity(y, ref, bound, what=f"config 3 packed={packed}")
+    assert qg.device_error() == 0
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_xreg_integer_inputs_exact(M):
+    # d = 1 and integer x in [-4, 4]: every product and partial sum is an
+    # integer times one power of two, below 2^24 of it: the result is exact.
+    rng = np.random.default_rng(77 + M)
+    N, K = 96, 4096
+    nb = K // 32
+    q = rng.integers(0, 16, size=(N, nb, 32)).astype(np.uint8)
+    w = synth.q4_0_from_parts(np.full((N, nb), 0x3C00, np.uint16), q)
+    x = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    y = qg.qgemv_q4_0(to_dev(w), to_dev(x), N=N)
+    exact = (x.astype(np.int64) @ (q.reshape(N, K).astype(np.int64) - 8).T).astype(np.float32)
+    assert_bitwise(y, exact, "integer closed form")
+
+
+@pytest.mark.parametrize("scale", [2.0 ** 110, 2.0 ** 100, 2.0 ** -100, 2.0 ** 60, 2.0 ** -60])
+def test_xreg_extreme_activation_magnitudes(scale):
+    M, N, K = 2, 40, 4096
+    c = synth.q4_0_case(5300, N, K, M)
+    x = (c["x"].astype(np.float64) * scale).astype(np.float32)
+    y = qg.qgemv_q4_0(to_dev(c["w"]), to_dev(x), N=N)
+    ref, bound = oracle.gemv_q4_0(c["w"], x, M, N, K)
+    assert_parity(y, ref, bound, what=f"q4_0 x*{scale:g}")
+    ck = synth.q4_k_case(5301, N, K, M)
+    xk = (ck["x"].astype(np.float64) * scale).astype(np.float32)
+    y = qg.qgemv_q4_k(to_dev(ck["w"]), to_dev(xk), N=N)
+    ref, bound = oracle.gemv_q4_k(ck["w"], xk, M, N, K)
+    assert_parity(y, ref, bound, what=f"q4_k x*{scale:g}")
+
+
+def test_xreg_wide_activation_range_and_zeros():
+    # One large element sets the power of two for the whole row; the rest
+    # spans 2^-60 .. 2^10. Row 1 is all zeros (the result must be exactly 0).
+    M, N, K = 2, 33, 4096
+    c = synth.q4_0_case(5400, N, K, M)
+    rng = np.random.default_rng(5)
+    x = np.zeros((M, K), np.float32)
+    x[0] = (rng.standard_normal(K) * 2.0 ** rng.integers(-60, 10, K)).astype(np.float32)
+    x[0, 17] = 3.0e5
+    y = qg.qgemv_q4_0(to_dev(c["w"]), to_dev(x), N=N)
+    ref, bound = oracle.gemv_q4_0(c["w"], x, M, N, K)
+    assert_parity(y, ref, bound, what="wide-range x")
+    assert not y[1].any()
+
+
+def test_xreg_non_finite_activation_propagates():
+    M, N, K = 1, 20, 1024
+    c = synth.q4_0_case(5500, N, K, M)
+    for bad in (np.inf, np.nan):
+        x = c["x"].copy()
+        x[0, 100] = bad
+        y = qg.qgemv_q4_0(to_dev(c["w"]), to_dev(x), N=N).cpu().numpy()
+        assert not np.isfinite(y).any(), bad
+
+
+@pytest.mark.parametrize("ahead", [1, 2, 5])
+def test_xreg_ahead_does_not_change_results(ahead):
+    M, N, K = 1, 700, 4096
+    c = synth.q4_0_case(5600 + ahead, N, K, M, dual=True)
+    wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
+    base = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    qg.set_option(qg.QG_OPT_XREG_AHEAD, ahead)
+    try:
+        ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    finally:
+        qg.set_option(qg.QG_OPT_XREG_AHEAD, 0)
+    assert_bitwise(ya, base[0], f"ahead={ahead} y_a")
+    assert_bitwise(yb, base[1], f"ahead={ahead} y_b")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_xreg_agrees_with_staged_kernel(M):
+    N, K = 257, 4096
+    c = synth.q4_k_case(5700 + M, N, K, M)
+    w, x = to_dev(c["w"]), to_dev(c["x"])
+    y_new = qg.qgemv_q4_k(w, x, N=N)
+    qg.set_option(qg.QG_OPT_XREG, 0)
+    try:
+        y_old = qg.qgemv_q4_k(w, x, N=N)
+    finally:
+        qg.set_option(qg.QG_OPT_XREG, 1)
+    _, bound = oracle.gemv_q4_k(c["w"], c["x"], M, N, K)
+    # Both are within the bound of the exact value, so within twice of each other.
+    assert_parity(y_new, y_old.cpu().numpy().astype(np.float64), bound, rel=2e-5, abs_=2e-6,
+                  what="xreg vs staged")
+
+
+def test_xreg_pdl_chain_at_full_size():
+    """Back-to-back calls under programmatic dependent launch, each reading the
+    previous call's output as its x (the decode-layer pattern)."""
+    N = K = 4096
+    c = synth.q4_0_case(5800, N, K, 1, dual=True)
+    ck = synth.q4_k_case(5801, N, K, 1)
+    wa, wb, wk = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(ck["w"])
+    qg.set_option(qg.QG_OPT_PDL, 1)
+    try:
+        ya, yb = qg.qgemv_dual_q4_0(wa, wb, to_dev(c["x"]), N=N)
+        y2 = qg.qgemv_q4_k(wk, yb, N=N)
+        y3, y4 = qg.qgemv_dual_q4_0(wa, wb, y2, N=N)
+        torch.cuda.synchronize()
+    finally:
+        qg.set_option(qg.QG_OPT_PDL, 0)
+    _, (rb, bb) = oracle.gemv_dual_q4_0(c["w"], c["w_b"], c["x"], 1, N, K)
+    assert_parity(yb, rb, bb, what="chain 1")
+    r2, b2 = oracle.gemv_q4_k(ck["w"], yb.cpu().numpy(), 1, N, K)
+    assert_parity(y2, r2, b2, what="chain 2")
+    (r3, b3), _ = oracle.gemv_dual_q4_0(c["w"], c["w_b"], y2.cpu().numpy(), 1, N, K)
+    assert_parity(y3, r3, b3, what="chain 3")
+    assert qg.device_error() == 0
+
+
+def test_xreg_independent_calls_mode():
+    """QG_OPT_PDL = 2: consecutive calls that neither read nor write each
+    other's buffers run concurrently; every output is bitwise what the same
+    call gives alone."""
+    N = K = 4096
+    cases = [synth.q4_0_case(5900 + i, N, K, 1, dual=True) for i in range(3)]
+    ws = [(to_dev(c["w"]), to_dev(c["w_b"])) for c in cases]
+    x = to_dev(cases[0]["x"])
+    alone = [qg.qgemv_dual_q4_0(wa, wb, x, N=N) for wa, wb in ws]
+    torch.cuda.synchronize()
+    outs = [(torch.empty((1, N), device="cuda"), torch.empty((1, N), device="cuda"))
+            for _ in range(12)]
+    qg.set_option(qg.QG_OPT_PDL, 2)
+    try:
+        for i, (ya, yb) in enumerate(outs):
+            wa, wb = ws[i % 3]
+            qg.qgemv_dual_q4_0(wa, wb, x, ya, yb, N=N)
+        torch.cuda.synchronize()
+    finally:
+        qg.set_option(qg.QG_OPT_PDL, 0)
+    for i, (ya, yb) in enumerate(outs):
+        assert_bitwise(ya, alone[i % 3][0], f"independent call {i} y_a")
+        assert_bitwise(yb, alone[i % 3][1], f"independent call {i} y_b")
+    assert qg.device_error() == 0
+
+
+@pytest.fixture(params=["8 warps", "4 warps"])
+def cta_shape(request):
+    """The kernel's two CTA shapes: eight consumer warps (two CTAs per SM) and
+    four (four CTAs per SM, taken automatically for independent calls)."""
+    qg.set_option(qg.QG_OPT_XREG_WARPS, 4 if request.param == "4 warps" else 0)
+    yield request.param
+    qg.set_option(qg.QG_OPT_XREG_WARPS, 0)
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K", [(37, 256), (61, 1024), (70, 3072), (300, 4096)])
+def test_xreg_cta_shapes_q4_0(M, N, K, cta_shape):
+    c = synth.q4_0_case(6000 + 7 * M + N, N, K, M, dual=True)
+    wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
+    ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    assert_bitwise(ya, qg.qgemv_q4_0(wa, x, N=N), f"{cta_shape} dual vs single")
+    (ra, ba), (rb, bb) = oracle.gemv_dual_q4_0(c["w"], c["w_b"], c["x"], M, N, K)
+    assert_parity(ya, ra, ba, what=f"{cta_shape} y_a M={M} N={N} K={K}")
+    assert_parity(yb, rb, bb, what=f"{cta_shape} y_b M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_xreg_cta_shapes_q4_k_and_affine(M, cta_shape):
+    N, K = 129, 4096
+    c = synth.q4_k_case(6100 + M, N, K, M)
+    y = qg.qgemv_q4_k(to_dev(c["w"]), to_dev(c["x"]), N=N)
+    assert_parity(y, *oracle.gemv_q4_k(c["w"], c["x"], M, N, K), what=f"{cta_shape} q4_k")
+    c = synth.affine_case(6200 + M, N, K, M, 64)
+    x, s, b = to_dev(c["x"]), to_dev(c["s"]), to_dev(c["b"])
+    yu = qg.qmm_affine(x, to_dev(c["q"]), s, b, 64, 0)
+    yp = qg.qmm_affine(x, to_dev(c["q_packed"]), s, b, 64, 1)
+    assert_bitwise(yp, yu, f"{cta_shape} packed vs u8")
+    ref, bound = oracle.qmm_affine(c["x"], c["q"], c["s"], c["b"], M, N, K, 64, False)
+    assert_parity(yu, ref, bound, what=f"{cta_shape} affine")
+
+
+def test_xreg_cta_shape_does_not_change_results():
+    """Each output's arithmetic depends on the format, M, K and x only: the
+    two CTA shapes give bitwise the same y."""
+    N, K = 777, 4096
+    c = synth.q4_0_case(6300, N, K, 1, dual=True)
+    wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
+    base = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+    qg.set_option(qg.QG_OPT_XREG_WARPS, 4)
+    try:
+        for ctas in (1, 2, 4):
+            qg.set_option(qg.QG_OPT_XREG_CTAS, ctas)
+            ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+            assert_bitwise(ya, base[0], f"4 warps, {ctas} CTAs per SM, y_a")
+            assert_bitwise(yb, base[1], f"4 warps, {ctas} CTAs per SM, y_b")
+    finally:
+        qg.set_option(qg.QG_OPT_XREG_WARPS, 0)
+        qg.set_option(qg.QG_OPT_XREG_CTAS, 1)
