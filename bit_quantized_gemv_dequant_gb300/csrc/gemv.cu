@@ -443,10 +443,10 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // Partial sums, then the staging area of x (Mc * K floats).
     const long long red_floats = (rbuf * Mc * WG + 3) & ~3ll;
     const long long fixed = (red_floats + (long long)Mc * a.K) * 4 + (long long)NWC * Mc * 4 + 128;
-    // Eight consumer warps with one input row fit twice on an SM (this call's
-    // CTA and the next one's); otherwise one CTA per SM.
-    // Four consumer warps: four CTAs per SM.
-    const bool co = (NWC == 8 && Mc == 1) || NWC == 4;
+    // Eight or twelve consumer warps with one input row fit twice on an SM
+    // (this call's CTA and the next one's), four consumer warps four times;
+    // otherwise one CTA per SM.
+    const bool co = ((NWC == 8 || NWC == 12) && Mc == 1) || NWC == 4;
     const int per_sm = NWC == 4 ? 4 : 2;
     long long budget = co ? (long long)dc.smem_per_sm / per_sm - dc.reserved_smem : dc.max_smem_optin;
     long long S = std::min<long long>(16, (budget - fixed) / per_slot);

@@ -44,9 +44,9 @@
 //  * Programmatic dependent launch: the producer issues the first weight
 //    copies before the kernel waits for its predecessor; consumers wait
 //    (griddepcontrol.wait) before they read x and before any y is written.
-//    With eight consumer warps and M = 1 the CTA uses at most half an SM's
-//    registers and shared memory, so the next call's CTA can stream its
-//    weights while this one computes.
+//    With eight or twelve consumer warps and M = 1 the CTA uses at most half
+//    an SM's registers and shared memory (four warps: a quarter), so the next
+//    call's CTA can stream its weights while this one computes.
 //
 // Every output's arithmetic depends only on (format, M, K, x), never on N, the
 // matrix count, the grid or the chunk: the dual projection is bitwise equal to
@@ -197,48 +197,13 @@ __device__ __forceinline__ Chunk chunk_at(int r, int re, int N, int RC) {
     return Chunk{wi, row0, min(min(re - r, RC), N - row0)};
 }
 
-// Consumer warps of one Q4_0 parity class (PAR), or of another format (PAR 0).
-template <int FMT, int MT, int NWC, int RPG, int PAR>
-__device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t* full,
-                                       uint64_t* empty, float* red, float* xst, float* xmax,
-                                       int warp, int lane) {
-    constexpr int V = MT * RPG;
-    constexpr bool kAffine = (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED);
-    const int grp = warp / p.WG, gw = warp - grp * p.WG;
-    const bool in_group = grp < p.NRG;
-
-    // ------------------------------------------------- this lane's K unit
-    int u;
-    if (FMT == FMT_Q4_0) u = 64 * (gw >> 1) + 2 * lane + PAR;
-    else u = gw * 32 + lane;
-    const bool valid = in_group && u < p.units;
-    const int uu = valid ? u : 0;
-    int qoff, hoff = 0;
-    if (FMT == FMT_Q4_0) {
-        qoff = (18 * uu) & ~3;
-    } else if (FMT == FMT_Q4_K) {
-        const int sb = uu >> 3, j = uu & 7;
-        qoff = 144 * sb + 16 + 16 * j;
-        hoff = 144 * sb;
-    } else {
-        qoff = (FMT == FMT_AFF_U8 ? 32 : 16) * uu;
-    }
-    const int grp_s = kAffine ? ((32 * uu) >> p.log2gs) : 0;
-    // Q4_K: the scale pair this lane decodes (sub-block j = unit % 8) and the
-    // constants that make the 6-bit field extraction branch-free.
-    const int j8 = uu & 7, hh = uu & 1;
-    const uint32_t k_mlo = j8 < 4 ? 63u : 15u, k_shm = j8 < 4 ? 0u : 4u;
-    const uint32_t k_shh = j8 < 4 ? 0u : (uint32_t)(8 * j8 - 30), k_mh = j8 < 4 ? 0u : 0x30u;
-
-    // x and y may be produced / consumed by the preceding kernel (unless the
-    // caller declared the calls independent).
-    if (p.dep_wait) pdl_wait();
-
-    // ------------------------------------------------------- load x
-    // All consumer threads load x with coalesced 16-byte loads into shared
-    // memory, laid out per lane unit (8 float4 chunks in the lane's pair order,
-    // chunk j stored at j ^ (reader lane & 7), so that the lanes' reads below
-    // are conflict-free), and track max |x| on the way.
+// All consumer threads load x with coalesced 16-byte loads into shared memory,
+// laid out per lane unit (8 float4 chunks in the lane's pair order, chunk j
+// stored at j ^ (reader lane & 7), so that the lanes' reads are
+// conflict-free), and each warp writes its max |x| per input row to xmax.
+template <int FMT, int MT, int NWC>
+__device__ __forceinline__ void stage_x(const Params& p, float* xst, float* xmax, int warp,
+                                        int lane) {
     const int nthr_all = NWC * 32, tid_all = warp * 32 + lane;
     float4* xs4 = reinterpret_cast<float4*>(xst);
     const int q4n = p.K >> 2;
@@ -279,6 +244,52 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
             amax[m] = fmaxf(amax[m], __shfl_xor_sync(0xffffffffu, amax[m], off));
         if (lane == 0) xmax[warp * MT + m] = amax[m];
     }
+}
+
+// Consumer warps of one Q4_0 parity class (PAR), or of another format (PAR 0).
+template <int FMT, int MT, int NWC, int RPG, int PAR>
+__device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t* full,
+                                       uint64_t* empty, float* red, float* xst, float* xmax,
+                                       int warp, int lane) {
+    constexpr int V = MT * RPG;
+    constexpr bool kAffine = (FMT == FMT_AFF_U8 || FMT == FMT_AFF_PACKED);
+    const int grp = warp / p.WG, gw = warp - grp * p.WG;
+    const bool in_group = grp < p.NRG;
+
+    // ------------------------------------------------- this lane's K unit
+    int u;
+    if (FMT == FMT_Q4_0) u = 64 * (gw >> 1) + 2 * lane + PAR;
+    else u = gw * 32 + lane;
+    // A lane past the end of a row (narrow K) gets x = 0 and reads a unit of
+    // the row with its own layout (a Q4_0 block of its parity), so that it
+    // adds exactly zero, or NaN only to a row whose exact result is not
+    // finite anyway (a non-finite scale in that unit).
+    const bool valid = in_group && u < p.units;
+    const int uu = valid ? u : (FMT == FMT_Q4_0 ? PAR : 0);
+    int qoff, hoff = 0;
+    if (FMT == FMT_Q4_0) {
+        qoff = (18 * uu) & ~3;
+    } else if (FMT == FMT_Q4_K) {
+        const int sb = uu >> 3, j = uu & 7;
+        qoff = 144 * sb + 16 + 16 * j;
+        hoff = 144 * sb;
+    } else {
+        qoff = (FMT == FMT_AFF_U8 ? 32 : 16) * uu;
+    }
+    const int grp_s = kAffine ? ((32 * uu) >> p.log2gs) : 0;
+    // Q4_K: the scale pair this lane decodes (sub-block j = unit % 8) and the
+    // constants that make the 6-bit field extraction branch-free.
+    const int j8 = uu & 7, hh = uu & 1;
+    const uint32_t k_mlo = j8 < 4 ? 63u : 15u, k_shm = j8 < 4 ? 0u : 4u;
+    const uint32_t k_shh = j8 < 4 ? 0u : (uint32_t)(8 * j8 - 30), k_mh = j8 < 4 ? 0u : 0x30u;
+
+    // x and y may be produced / consumed by the preceding kernel (unless the
+    // caller declared the calls independent). x is staged while the producer
+    // issues the weight copies.
+    if (p.dep_wait) pdl_wait();
+    stage_x<FMT, MT, NWC>(p, xst, xmax, warp, lane);
+    const int q4n = p.K >> 2;
+    const float4* xs4 = reinterpret_cast<const float4*>(xst);
     named_bar_sync(1, NWC * 32);
     int S_[MT];
 #pragma unroll
@@ -392,8 +403,8 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
                 uint32_t wd[5];
 #pragma unroll
                 for (int t = 0; t < 5; ++t) wd[t] = wp[t];
-                const float d = __half2float(__ushort_as_half(
-                    (unsigned short)(PAR ? (wd[0] >> 16) : (wd[0] & 0xFFFFu))));
+                const __half2 dh = *reinterpret_cast<const __half2*>(&wd[0]);
+                const float d = PAR ? __high2float(dh) : __low2float(dh);
                 // Two chains (even and odd pairs) halve the dependent FMA depth.
                 float2 acc[MT][2];
 #pragma unroll
@@ -467,8 +478,6 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
                     o[m] = __fmaf_rn(sc, t.x + t.y, bi * xoff[m]);
                 }
             }
-#pragma unroll
-            for (int m = 0; m < MT; ++m) o[m] = valid ? o[m] : 0.0f;  // narrow K: lanes past the row
         };
         // The group's RPG rows in one straight-line block, then one
         // transposing butterfly for all of them. In a short chunk (the end of
@@ -503,7 +512,8 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
 }
 
 template <int FMT, int MT, int NWC, int RPG>
-__global__ void __launch_bounds__((NWC + 1) * 32, NWC == 4 ? 4 : (NWC == 8 && MT == 1) ? 2 : 1)
+__global__ void __launch_bounds__((NWC + 1) * 32,
+                                  NWC == 4 ? 4 : ((NWC == 8 || NWC == 12) && MT == 1) ? 2 : 1)
     gemv_xreg_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ring = smem;
