@@ -340,6 +340,9 @@ def sweep_specs():
         ("cfg3 affine packed M=512 folded", lambda: make_single("affine", 512, 4096, 4096, 3, 64, 1)),
         ("prefill dual q4_0 N=K=4096 M=512 folded", lambda: make_dual_q4_0(512, 4096, 4096, 80)),
         ("prefill q4_k N=K=4096 M=512 folded", lambda: make_single("q4_k", 512, 4096, 4096, 81)),
+        # 8 < M < 64 on the CUDA cores (f32 bar), against the f32 FMA roofline.
+        ("mid-M dual q4_0 N=K=4096 M=16", lambda: make_dual_q4_0(16, 4096, 4096, 85)),
+        ("mid-M dual q4_0 N=K=4096 M=32", lambda: make_dual_q4_0(32, 4096, 4096, 85)),
     ]
     for M in (1, 2, 4, 8):
         specs += [

@@ -23,7 +23,7 @@ std::once_flag g_once[kMaxDevices];
 int g_ctx_rc[kMaxDevices];
 thread_local int t_last_cuda_error = 0;
 std::atomic<long long> g_opt_pdl{0};
-std::atomic<long long> g_opt_prefill_min_m{16};
+std::atomic<long long> g_opt_prefill_min_m{64};
 std::atomic<long long> g_opt_stream{1};
 std::atomic<long long> g_opt_stream_warps{0};
 std::atomic<long long> g_opt_stream_slots{0};

@@ -97,7 +97,7 @@ enum {
  *
  * Q4_0 and Q4_K calls take one of two paths:
  * - CUDA cores, f32 (|y - exact| <= 1e-5 * sum_k |x w| + 1e-6), for every M.
- * - Tensor cores (prefill), when M >= QG_OPT_PREFILL_MIN_M (default 16), x is
+ * - Tensor cores (prefill), when M >= QG_OPT_PREFILL_MIN_M (default 64), x is
  *   16-byte aligned, the tensor-core prefill conditions of qmm_affine hold for
  *   group size 32, and the workspace is at least qg_workspace_size bytes. The
  *   weights are rewritten in the workspace as packed affine codes per 32
@@ -157,7 +157,7 @@ QG_API int qgemv_q4_k_noalloc(const void* w, const float* x, float* y, int64_t M
  *
  * Two paths, chosen per call:
  * - CUDA cores, f32 throughout (|y - exact| <= 1e-5 * sum_k |x w| + 1e-6):
- *   M below the QG_OPT_PREFILL_MIN_M option (default 16), or any of the
+ *   M below the QG_OPT_PREFILL_MIN_M option (default 64), or any of the
  *   tensor-core conditions below unmet.
  * - Tensor cores (prefill), when M >= QG_OPT_PREFILL_MIN_M, group_size >= 16,
  *   K % 16 == 0 (K % 32 == 0 when packed), q and x 16-byte aligned, M, N, K
@@ -246,8 +246,9 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * kernels behave as with 1. A kernel launched after such a call without
  * programmatic dependent launch still waits for it as usual. */
 /*
- * QG_OPT_PREFILL_MIN_M (default 16, >= 1): smallest M for which qmm_affine
- * takes the tensor-core prefill path (when its other conditions hold). */
+ * QG_OPT_PREFILL_MIN_M (default 64, >= 1): smallest M for which qmm_affine
+ * (and the Q4_0 / Q4_K calls) take the tensor-core prefill path when its
+ * other conditions hold. Below it every call keeps the f32 bound. */
 /*
  * QG_OPT_STREAM (default 1): which GEMV/qmm calls with M <= 2 (per slice of
  * x) take the streaming kernel instead of the staged-stage kernel. 0: none.

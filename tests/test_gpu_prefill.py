@@ -32,6 +32,16 @@ pytestmark = pytest.mark.gpu
 REL_TC = oracle.REL_TC
 
 
+@pytest.fixture(autouse=True)
+def tensor_cores_from_m16():
+    """These tests exercise the tensor-core prefill at small M on purpose: the
+    threshold is lowered to 16 for them (the library's default is 64)."""
+    old = qg.get_option(qg.QG_OPT_PREFILL_MIN_M)
+    qg.set_option(qg.QG_OPT_PREFILL_MIN_M, 16)
+    yield
+    qg.set_option(qg.QG_OPT_PREFILL_MIN_M, old)
+
+
 @pytest.fixture
 def min_m():
     old = qg.get_option(qg.QG_OPT_PREFILL_MIN_M)

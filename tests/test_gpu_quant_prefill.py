@@ -21,6 +21,7 @@ from bit_quantized_gemv_dequant_gb300 import synth
 
 from helpers import assert_bitwise, assert_parity, dev, to_dev
 from test_gpu_prefill import REL_TC, _rounded_x, kernel, rounded_ref  # noqa: F401 (fixture)
+from test_gpu_prefill import tensor_cores_from_m16  # noqa: F401 (autouse fixture)
 
 pytestmark = pytest.mark.gpu
 
