@@ -494,9 +494,9 @@ def e2e_dual(steps: int, warmup: int, M: int = 1, N: int = 4096, K: int = 4096):
 
 
 # -------------------------------------------------------------- traffic
-TRAFFIC_SOURCES = ("bit_quantized_gemv_dequant_gb300/csrc/gemv_fast.cuh",
+TRAFFIC_SOURCES = ("bit_quantized_gemv_dequant_gb300/csrc/gemv_xreg.cuh",
                    "bit_quantized_gemv_dequant_gb300/csrc/gemv.cu",
-                   "bit_quantized_gemv_dequant_gb300/csrc/gemv_fast_q4_0.cu",
+                   "bit_quantized_gemv_dequant_gb300/csrc/gemv_xreg_q4_0.cu",
                    "bit_quantized_gemv_dequant_gb300/csrc/qg_internal.cuh")
 
 
@@ -730,7 +730,7 @@ def main():
                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                         if peak_src == "measured" else "fallback 6.8 TB/s",
                         "unit": "GB/s", "frac": achieved / hbm_peak,
-                        "traffic": recorded_traffic("gemv_q4_0_dual_m1")},
+                        "traffic": recorded_traffic("dual_q4_0_m1_n4096_k4096")},
            "clocks": clocks}
 
     out["launch_mode"] = {
