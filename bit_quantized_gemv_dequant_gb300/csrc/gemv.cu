@@ -395,7 +395,8 @@ struct XPlan {
 XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x) {
     XPlan xp{};
     xp.ok = false;
-    if (Mc > 2 || launch_option(QG_OPT_XREG) == 0) return xp;
+    if (Mc > 4 || launch_option(QG_OPT_XREG) == 0) return xp;
+    const int MT = Mc <= 2 ? Mc : 4;  // three rows run as four (one of zeros)
     const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
     if (a.K % 32 || a.K > 16384) return xp;
     const long long units = a.K / 32;
@@ -413,6 +414,13 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     if (!aligned16(x)) return xp;
     if (affine && (!aligned16(a.scales) || !aligned16(a.biases))) return xp;
     if ((long long)a.nw * a.N >= (1ll << 31)) return xp;
+    if (MT == 4 && (WG > 4 || 4 % WG)) return xp;  // four x rows: only four consumer warps fit
+    // Four rows of x at once (one CTA of four consumer warps per SM) measured
+    // faster than the staged kernel for Q4_K and affine weights (M = 4 / 8:
+    // Q4_K 22.0 / 43.9 us against 24.3 / 47.4 us at N = 12288; affine u8
+    // 19.2 against 22.9 us at M = 8) but slower for Q4_0 (dual M = 4:
+    // 15.5 against 13.8 us), which keeps the staged kernel.
+    if (MT == 4 && a.fmt == FMT_Q4_0) return xp;
     int NWC = (8 % WG == 0) ? 8 : (12 % WG == 0) ? 12 : 16;
     // Four consumer warps (four CTAs, i.e. four calls, per SM) when calls are
     // declared independent (QG_OPT_PDL = 2): consecutive calls then overlap,
@@ -421,9 +429,9 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // eight warps (two CTAs per SM: this call's and the next one's).
     const long long want_w = launch_option(QG_OPT_XREG_WARPS);
     if (WG <= 4 && 4 % WG == 0 &&
-        (want_w == 4 || (want_w == 0 && launch_option(QG_OPT_PDL) == 2)))
+        (MT == 4 || want_w == 4 || (want_w == 0 && launch_option(QG_OPT_PDL) == 2)))
         NWC = 4;
-    if (NWC == 16 && Mc == 2) return xp;  // two x rows need more registers than 17 warps allow
+    if (NWC == 16 && MT == 2) return xp;  // two x rows need more registers than 17 warps allow
     const int NRG = std::min<int>(8, NWC / (int)WG);
     const int RC = NRG * xreg::kRPG;
     const long long rb = row_bytes(a.fmt, a.K);
@@ -438,16 +446,16 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     const long long ctas_per_sm = std::max<long long>(1, launch_option(QG_OPT_XREG_CTAS));
     const long long grid_max = (long long)dc.num_sms * ctas_per_sm;
     const long long rows_cta = ((long long)a.nw * a.N + grid_max - 1) / grid_max;
-    const long long rbuf = std::max<long long>(RC, std::min<long long>(rows_cta, 4096 / (Mc * WG)));
+    const long long rbuf = std::max<long long>(RC, std::min<long long>(rows_cta, 4096 / (MT * WG)));
     const long long per_slot = slot + 16;
-    // Partial sums, then the staging area of x (Mc * K floats).
-    const long long red_floats = (rbuf * Mc * WG + 3) & ~3ll;
-    const long long fixed = (red_floats + (long long)Mc * a.K) * 4 + (long long)NWC * Mc * 4 + 128;
+    // Partial sums, then the staging area of x (MT * K floats).
+    const long long red_floats = (rbuf * MT * WG + 3) & ~3ll;
+    const long long fixed = (red_floats + (long long)MT * a.K) * 4 + (long long)NWC * MT * 4 + 128;
     // Eight or twelve consumer warps with one input row fit twice on an SM
-    // (this call's CTA and the next one's), four consumer warps four times;
-    // otherwise one CTA per SM.
-    const bool co = ((NWC == 8 || NWC == 12) && Mc == 1) || NWC == 4;
-    const int per_sm = NWC == 4 ? 4 : 2;
+    // (this call's CTA and the next one's), four consumer warps four times
+    // (three times with two input rows); otherwise one CTA per SM.
+    const bool co = ((NWC == 8 || NWC == 12) && MT == 1) || (NWC == 4 && MT <= 2);
+    const int per_sm = NWC == 4 ? (MT == 1 ? 4 : 3) : 2;
     long long budget = co ? (long long)dc.smem_per_sm / per_sm - dc.reserved_smem : dc.max_smem_optin;
     long long S = std::min<long long>(16, (budget - fixed) / per_slot);
     if ((budget - fixed) / (slot_fit + 16) < 2) {
@@ -502,7 +510,15 @@ int fast_launch_aff_u8(const DevCtx&, const fast::Params&, int, int, int, int, i
 int fast_launch_aff_packed(const DevCtx&, const fast::Params&, int, int, int, int, int, int,
                            bool, cudaStream_t);
 
+// Calls with more than two rows of x run in slices of four on the
+// register-resident-x kernel when it takes four rows for this shape (no
+// workspace), else in slices of eight on the staged kernel.
+bool xreg_four_row_slices(const DevCtx& dc, const GemvArgs& a) {
+    return a.M >= 3 && make_xreg_plan(dc, a, 4, a.x).ok;
+}
+
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a) {
+    if (xreg_four_row_slices(dc, a)) return 0;
     size_t worst = 0;
     for (long long m0 = 0; m0 < a.M; m0 += 8) {
         const int Mc = (int)std::min<long long>(8, a.M - m0);
@@ -515,8 +531,9 @@ size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a) {
 
 int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s) {
     const bool affine = (a.fmt == FMT_AFF_U8 || a.fmt == FMT_AFF_PACKED);
-    for (long long m0 = 0; m0 < a.M; m0 += 8) {
-        const int Mc = (int)std::min<long long>(8, a.M - m0);
+    const int step = xreg_four_row_slices(dc, a) ? 4 : 8;
+    for (long long m0 = 0; m0 < a.M; m0 += step) {
+        const int Mc = (int)std::min<long long>(step, a.M - m0);
         const float* x = a.x + m0 * a.K;
         float* y0 = a.y[0] + m0 * a.N;
         float* y1 = (a.nw > 1 ? a.y[1] : a.y[0]) + m0 * a.N;
@@ -555,18 +572,19 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
             const long long pdl_mode = launch_option(QG_OPT_PDL);
             const bool pdl = pdl_mode != 0;
             kp.dep_wait = pdl_mode == 2 ? 0 : 1;
+            const int MT = Mc <= 2 ? Mc : 4;
             switch (a.fmt) {
                 case FMT_Q4_0:
-                    rc = xreg_launch_q4_0(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    rc = xreg_launch_q4_0(dc, kp, MT, xp.NWC, xp.grid, xp.smem, pdl, s);
                     break;
                 case FMT_Q4_K:
-                    rc = xreg_launch_q4_k(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    rc = xreg_launch_q4_k(dc, kp, MT, xp.NWC, xp.grid, xp.smem, pdl, s);
                     break;
                 case FMT_AFF_U8:
-                    rc = xreg_launch_aff_u8(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    rc = xreg_launch_aff_u8(dc, kp, MT, xp.NWC, xp.grid, xp.smem, pdl, s);
                     break;
                 default:
-                    rc = xreg_launch_aff_packed(dc, kp, Mc, xp.NWC, xp.grid, xp.smem, pdl, s);
+                    rc = xreg_launch_aff_packed(dc, kp, MT, xp.NWC, xp.grid, xp.smem, pdl, s);
                     break;
             }
             if (rc != QG_OK) return rc;

@@ -211,13 +211,16 @@ __device__ __forceinline__ void stage_x(const Params& p, float* xst, float* xmax
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         amax[m] = 0.0f;
-        const float4* xr = reinterpret_cast<const float4*>(p.x + (long long)m * p.K);
+        // A launch of four input rows may carry fewer (M = 3): the missing
+        // rows are zeros, computed but never stored.
+        const bool row_ok = m < p.M;
+        const float4* xr = reinterpret_cast<const float4*>(p.x + (long long)(row_ok ? m : 0) * p.K);
         for (int q0 = tid_all; q0 < q4n; q0 += 4 * nthr_all) {
             float4 t[4];
 #pragma unroll
             for (int i2 = 0; i2 < 4; ++i2) {
                 const int q = q0 + i2 * nthr_all;
-                t[i2] = q < q4n ? xr[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+                t[i2] = (row_ok && q < q4n) ? xr[q] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int i2 = 0; i2 < 4; ++i2) {
@@ -379,7 +382,7 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
             for (int g2 = 1; g2 < WG; ++g2) t += src[g2];
             const int ra = fb + lr;
             const int wi = ra >= N ? 1 : 0;
-            p.out[wi][(long long)m * N + (ra - wi * N)] = t * dsc1[m] * dsc2[m];
+            if (m < p.M) p.out[wi][(long long)m * N + (ra - wi * N)] = t * dsc1[m] * dsc2[m];
         }
         if (!last) named_bar_sync(2, nthr);
         fb = upto;
@@ -513,7 +516,10 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
 
 template <int FMT, int MT, int NWC, int RPG>
 __global__ void __launch_bounds__((NWC + 1) * 32,
-                                  NWC == 4 ? 4 : ((NWC == 8 || NWC == 12) && MT == 1) ? 2 : 1)
+                                  MT == 4   ? 1
+                                  : NWC == 4 ? (MT == 1 ? 4 : 3)
+                                  : ((NWC == 8 || NWC == 12) && MT == 1) ? 2
+                                             : 1)
     gemv_xreg_kernel(const Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ring = smem;
@@ -666,10 +672,16 @@ int dispatch(const DevCtx& dc, const Params& kp, int MT, int NWC, int grid, int 
         if (NWC == 12) return launch<FMT, 1, 12, kRPG>(dc, kp, grid, smem, pdl, s);
         return launch<FMT, 1, 16, kRPG>(dc, kp, grid, smem, pdl, s);
     }
-    // Two input rows with sixteen consumer warps would spill: not planned.
-    if (NWC == 4) return launch<FMT, 2, 4, kRPG>(dc, kp, grid, smem, pdl, s);
-    if (NWC == 8) return launch<FMT, 2, 8, kRPG>(dc, kp, grid, smem, pdl, s);
-    if (NWC == 12) return launch<FMT, 2, 12, kRPG>(dc, kp, grid, smem, pdl, s);
+    if (MT == 2) {
+        // Two input rows with sixteen consumer warps would spill: not planned.
+        if (NWC == 4) return launch<FMT, 2, 4, kRPG>(dc, kp, grid, smem, pdl, s);
+        if (NWC == 8) return launch<FMT, 2, 8, kRPG>(dc, kp, grid, smem, pdl, s);
+        if (NWC == 12) return launch<FMT, 2, 12, kRPG>(dc, kp, grid, smem, pdl, s);
+        return QG_ERR_UNSUPPORTED;
+    }
+    // Three or four input rows (128 registers of x per lane): four consumer
+    // warps, one CTA per SM.
+    if (NWC == 4) return launch<FMT, 4, 4, kRPG>(dc, kp, grid, smem, pdl, s);
     return QG_ERR_UNSUPPORTED;
 }
 

@@ -19,6 +19,16 @@ from helpers import assert_bitwise, assert_parity, dev, to_dev
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["default kernels", "staged kernel"])
+def kernel_choice(request):
+    """Every test here runs twice: with the library's default choice (the
+    register-resident-x kernel for M <= 8 where it applies) and with that
+    kernel switched off, so that the staged kernel keeps its coverage."""
+    qg.set_option(qg.QG_OPT_XREG, 0 if request.param == "staged kernel" else 1)
+    yield request.param
+    qg.set_option(qg.QG_OPT_XREG, 1)
+
+
 def _q4_0(case_id, M, N, K, dual=False, w_offset=0):
     c = synth.q4_0_case(case_id, N, K, M, dual=dual)
     d = {"w": to_dev(c["w"], w_offset), "x": to_dev(c["x"])}

@@ -280,3 +280,42 @@ def test_xreg_cta_shape_does_not_change_results():
     finally:
         qg.set_option(qg.QG_OPT_XREG_WARPS, 0)
         qg.set_option(qg.QG_OPT_XREG_CTAS, 1)
+
+
+@pytest.mark.parametrize("M", [3, 4, 5, 7, 8, 11])
+@pytest.mark.parametrize("N,K", [(37, 256), (61, 1024), (130, 4096)])
+def test_xreg_four_row_slices(M, N, K):
+    """Three to eight (and more) rows of x run in slices of four rows on this
+    kernel for Q4_K and affine weights with K <= 4096; a slice of three runs
+    with one row of zeros. (Q4_0 keeps the staged kernel for M >= 3.)"""
+    assert qg.workspace_size(qg.QG_OP_Q4_K, M, N, K) == 0
+    ck = synth.q4_k_case(6500 + M + N, N, K, M)
+    y = qg.qgemv_q4_k(to_dev(ck["w"]), to_dev(ck["x"]), N=N)
+    assert_parity(y, *oracle.gemv_q4_k(ck["w"], ck["x"], M, N, K), what=f"q4_k M={M} K={K}")
+    if K >= 256:
+        ca = synth.affine_case(6600 + M + N, N, K, M, 64)
+        xa, s_, b_ = to_dev(ca["x"]), to_dev(ca["s"]), to_dev(ca["b"])
+        yu = qg.qmm_affine(xa, to_dev(ca["q"]), s_, b_, 64, 0)
+        yp = qg.qmm_affine(xa, to_dev(ca["q_packed"]), s_, b_, 64, 1)
+        assert_bitwise(yp, yu, f"M={M} packed vs u8")
+        ref, bound = oracle.qmm_affine(ca["x"], ca["q"], ca["s"], ca["b"], M, N, K, 64, False)
+        assert_parity(yu, ref, bound, what=f"affine M={M} K={K}")
+    assert qg.device_error() == 0
+
+
+def test_xreg_four_rows_full_size():
+    """The decode sweep's M = 4 and 8 FFN-up Q4_K projection (N = 12288,
+    K = 4096) and config 3's affine M = 8, sampled rows."""
+    N, K = 12288, 4096
+    for M in (4, 8):
+        c = synth.q4_k_case(6700 + M, N, K, M)
+        y = qg.qgemv_q4_k(to_dev(c["w"]), to_dev(c["x"]), N=N)
+        rows = np.arange(3, N, 97)
+        ref, bound = oracle.gemv_q4_k(c["w"], c["x"], M, N, K, rows=rows)
+        assert_parity(y.cpu().numpy()[:, rows], ref[:, rows], bound[:, rows], what=f"q4_k M={M}")
+    c = synth.affine_case(6800, 4096, 4096, 8, 64)
+    y = qg.qmm_affine(to_dev(c["x"]), to_dev(c["q"]), to_dev(c["s"]), to_dev(c["b"]), 64, 0)
+    rows = np.arange(5, 4096, 61)
+    ref, bound = oracle.qmm_affine(c["x"], c["q"], c["s"], c["b"], 8, 4096, 4096, 64, False,
+                                   rows=rows)
+    assert_parity(y.cpu().numpy()[:, rows], ref[:, rows], bound[:, rows], what="affine M=8")
