@@ -774,7 +774,12 @@ def main():
                             "peak_source": f"{n_sm} SMs x 128 f32 FMA/clk x 2 x max SM clock"}})
     out["m8"] = m8
 
+    # A host round trip per step issues one call at a time: plain launches
+    # (each call then runs with eight consumer warps per CTA).
+    qg.set_option(qg.QG_OPT_PDL, 0)
     out["e2e"] = e2e_dual(min(2000, max(200, args.steps // 100)), 20)
+    out["e2e"]["launch_mode"] = "plain launches (QG_OPT_PDL = 0): one call per host round trip"
+    qg.set_option(qg.QG_OPT_PDL, args.pdl)
 
     if not args.no_cpu:
         gbs1, rows1, calls1, dt1 = oracle_dual_sample(1, 4096, 4096, budget_s=6.0)

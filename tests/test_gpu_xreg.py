@@ -319,3 +319,39 @@ def test_xreg_four_rows_full_size():
     ref, bound = oracle.qmm_affine(c["x"], c["q"], c["s"], c["b"], 8, 4096, 4096, 64, False,
                                    rows=rows)
     assert_parity(y.cpu().numpy()[:, rows], ref[:, rows], bound[:, rows], what="affine M=8")
+
+
+def test_decode_layer_chain_under_pdl():
+    """The decode layer's four full-size projections (Q+gate dual N = 4096,
+    K+V dual N = 1024, FFN up Q4_K N = 12288, FFN down Q4_K K = 12288) in
+    sequence under programmatic dependent launch, each reading the previous
+    call's output as its x (chained where the shapes allow), against the
+    oracle run on the same inputs."""
+    H, F = 4096, 12288
+    qgate = synth.q4_0_case(6900, H, H, 1, dual=True)
+    kv = synth.q4_0_case(6901, H // 4, H, 1, dual=True)
+    up = synth.q4_k_case(6902, F, H, 1)
+    down = synth.q4_k_case(6903, H, F, 1)
+    d = {k: to_dev(v) for k, v in (("qa", qgate["w"]), ("qb", qgate["w_b"]), ("ka", kv["w"]),
+                                   ("kb", kv["w_b"]), ("up", up["w"]), ("down", down["w"]))}
+    x0 = to_dev(qgate["x"])
+    qg.set_option(qg.QG_OPT_PDL, 1)
+    try:
+        q, g = qg.qgemv_dual_q4_0(d["qa"], d["qb"], x0, N=H)     # x of K+V and FFN up: q
+        k, v = qg.qgemv_dual_q4_0(d["ka"], d["kb"], q, N=H // 4)
+        u = qg.qgemv_q4_k(d["up"], q, N=F)                         # FFN up reads q
+        y = qg.qgemv_q4_k(d["down"], u, N=H)                       # FFN down reads u
+        torch.cuda.synchronize()
+    finally:
+        qg.set_option(qg.QG_OPT_PDL, 0)
+    (rq, bq), _ = oracle.gemv_dual_q4_0(qgate["w"], qgate["w_b"], qgate["x"], 1, H, H)
+    assert_parity(q, rq, bq, what="Q+gate")
+    qh = q.cpu().numpy()
+    (rk, bk), (rv, bv) = oracle.gemv_dual_q4_0(kv["w"], kv["w_b"], qh, 1, H // 4, H)
+    assert_parity(k, rk, bk, what="K")
+    assert_parity(v, rv, bv, what="V")
+    ru, bu = oracle.gemv_q4_k(up["w"], qh, 1, F, H)
+    assert_parity(u, ru, bu, what="FFN up")
+    ry, by = oracle.gemv_q4_k(down["w"], u.cpu().numpy(), 1, H, F)
+    assert_parity(y, ry, by, what="FFN down")
+    assert qg.device_error() == 0
