@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 QG_OK, QG_ERR_INVALID_ARG, QG_ERR_UNSUPPORTED, QG_ERR_MISALIGNED = 0, 1, 2, 3
 QG_ERR_CUDA, QG_ERR_WORKSPACE, QG_ERR_DEVICE = 4, 5, 6
 QG_OP_Q4_0, QG_OP_DUAL_Q4_0, QG_OP_Q4_K, QG_OP_AFFINE, QG_OP_AF4_G64 = 0, 1, 2, 3, 4
+QG_OP_DUAL_Q4_0_HOST = 5
 QG_OPT_PDL = 1
 QG_OPT_PREFILL_MIN_M = 2
 QG_OPT_STREAM, QG_OPT_STREAM_WARPS, QG_OPT_STREAM_SLOTS = 3, 4, 5
@@ -41,7 +42,7 @@ EXPORTS = ("qgemv_q4_0", "qgemv_dual_q4_0", "qgemv_q4_k", "qmm_affine", "qkv_spl
            "dequant_q4_0", "dequant_q4_k", "dequant_affine", "qg_workspace_size",
            "qg_status_string", "qg_last_cuda_error", "qg_device_error",
            "qg_selftest_wait_timeout", "qg_set_option", "qg_get_option",
-           "qgemv_q4_k_noalloc", "qg_prepare_af4_g64", "qmm_af4_g64")
+           "qgemv_q4_k_noalloc", "qg_prepare_af4_g64", "qmm_af4_g64", "qgemv_dual_q4_0_host")
 
 _LIB = None
 _LOCK = threading.Lock()
@@ -71,6 +72,7 @@ def lib():
         sig = {
             "qgemv_q4_0": [P, P, P, I64, I64, I64, P, SZ, P],
             "qgemv_dual_q4_0": [P, P, P, P, P, I64, I64, I64, P, SZ, P],
+            "qgemv_dual_q4_0_host": [P, P, P, P, P, I64, I64, I64, P, SZ, P],
             "qgemv_q4_k": [P, P, P, I64, I64, I64, P, SZ, P],
             "qmm_affine": [P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P],
             "qkv_split": [P, P, P, P, I64, I64, I64, I64, P],
@@ -111,6 +113,16 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _host(t: torch.Tensor, name: str, dtype) -> int:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
 
@@ -179,6 +191,28 @@ def qgemv_dual_q4_0(w_a, w_b, x, y_a=None, y_b=None, *, N=None, workspace=None, 
                                  _dev(x, "x", torch.float32), _dev(y_a, "y_a", torch.float32),
                                  _dev(y_b, "y_b", torch.float32), M, N, K, ws, wsb,
                                  st), "qgemv_dual_q4_0")
+    return y_a, y_b
+
+
+def qgemv_dual_q4_0_host(w_a, w_b, x, y_a=None, y_b=None, *, N=None, workspace=None,
+                         stream=None):
+    """qgemv_dual_q4_0 with x, y_a, y_b in host memory (CPU tensors); returns
+    once y_a and y_b hold the result. Page-locked buffers (pin_memory()) are
+    read and written in place for M <= 2; other buffers pass through device
+    staging. New outputs are page-locked when x is."""
+    M, K = x.shape
+    N = N if N is not None else w_a.numel() // (K // 32 * 18)
+    pin = x.is_pinned()
+    if y_a is None:
+        y_a = torch.empty((M, N), dtype=torch.float32, pin_memory=pin)
+    if y_b is None:
+        y_b = torch.empty((M, N), dtype=torch.float32, pin_memory=pin)
+    st = _stream(stream)
+    ws, wsb = _workspace(QG_OP_DUAL_Q4_0_HOST, M, N, K, 0, 0, w_a.device, workspace, st)
+    _check(lib().qgemv_dual_q4_0_host(_dev(w_a, "w_a", torch.uint8), _dev(w_b, "w_b", torch.uint8),
+                                      _host(x, "x", torch.float32), _host(y_a, "y_a", torch.float32),
+                                      _host(y_b, "y_b", torch.float32), M, N, K, ws, wsb, st),
+           "qgemv_dual_q4_0_host")
     return y_a, y_b
 
 

@@ -426,11 +426,21 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // declared independent (QG_OPT_PDL = 2): consecutive calls then overlap,
     // and more of them in flight hide each CTA's start-up and tail. A call
     // that waits for its predecessor computes alone, and does better with
-    // eight warps (two CTAs per SM: this call's and the next one's).
+    // eight warps (two CTAs per SM: this call's and the next one's). A call
+    // that runs alone keeps eight (measured against four and sixteen for the
+    // dual N = K = 4096 call: 17.2 us per host round trip against 18.8 and
+    // 18.0) and takes all of the SM's shared memory.
     const long long want_w = launch_option(QG_OPT_XREG_WARPS);
-    if (WG <= 4 && 4 % WG == 0 &&
-        (MT == 4 || want_w == 4 || (want_w == 0 && launch_option(QG_OPT_PDL) == 2)))
+    if (MT == 4) {
         NWC = 4;
+    } else if (want_w != 0) {
+        // A requested count that the row groups do not divide, or sixteen
+        // warps with two x rows (more registers than 17 warps allow), falls
+        // back to the automatic choice.
+        if (want_w % WG == 0 && !(want_w == 16 && MT == 2)) NWC = (int)want_w;
+    } else if (!a.isolated && WG <= 4 && 4 % WG == 0 && launch_option(QG_OPT_PDL) == 2) {
+        NWC = 4;
+    }
     if (NWC == 16 && MT == 2) return xp;  // two x rows need more registers than 17 warps allow
     const int NRG = std::min<int>(8, NWC / (int)WG);
     const int RC = NRG * xreg::kRPG;
@@ -454,7 +464,8 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // Eight or twelve consumer warps with one input row fit twice on an SM
     // (this call's CTA and the next one's), four consumer warps four times
     // (three times with two input rows); otherwise one CTA per SM.
-    const bool co = ((NWC == 8 || NWC == 12) && MT == 1) || (NWC == 4 && MT <= 2);
+    const bool co = !a.isolated &&
+                    (((NWC == 8 || NWC == 12) && MT == 1) || (NWC == 4 && MT <= 2));
     const int per_sm = NWC == 4 ? (MT == 1 ? 4 : 3) : 2;
     long long budget = co ? (long long)dc.smem_per_sm / per_sm - dc.reserved_smem : dc.max_smem_optin;
     long long S = std::min<long long>(16, (budget - fixed) / per_slot);
@@ -517,6 +528,18 @@ bool xreg_four_row_slices(const DevCtx& dc, const GemvArgs& a) {
     return a.M >= 3 && make_xreg_plan(dc, a, 4, a.x).ok;
 }
 
+// Every slice of the call runs on the register-resident-x kernel. That
+// kernel reads x with plain loads and writes y with plain stores and needs
+// no workspace, so x and y may then live in mapped host memory.
+bool gemv_xreg_only(const DevCtx& dc, const GemvArgs& a) {
+    const int step = xreg_four_row_slices(dc, a) ? 4 : 8;
+    for (long long m0 = 0; m0 < a.M; m0 += step) {
+        const int Mc = (int)std::min<long long>(step, a.M - m0);
+        if (!make_xreg_plan(dc, a, Mc, a.x + m0 * a.K).ok) return false;
+    }
+    return true;
+}
+
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a) {
     if (xreg_four_row_slices(dc, a)) return 0;
     size_t worst = 0;
@@ -569,7 +592,7 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
             kp.red_floats = xp.red_floats;
             kp.ahead = (int)std::min<long long>(launch_option(QG_OPT_XREG_AHEAD), xp.S);
             kp.err = dc.err;
-            const long long pdl_mode = launch_option(QG_OPT_PDL);
+            const long long pdl_mode = a.x_from_prev ? 1 : launch_option(QG_OPT_PDL);
             const bool pdl = pdl_mode != 0;
             kp.dep_wait = pdl_mode == 2 ? 0 : 1;
             const int MT = Mc <= 2 ? Mc : 4;

@@ -150,6 +150,107 @@ int run_gemv(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
     return gemv_launch(*dc, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Host-buffer calls stage x and the outputs in the workspace after the
+// call's own part: [call workspace | x | y_a | y_b], each part starting on a
+// 256-byte boundary (relative to the workspace's start).
+size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
+size_t host_stage_offset(size_t call_bytes) { return round256(call_bytes); }
+size_t host_stage_bytes(const GemvArgs& a) {
+    return round256((size_t)(a.M * a.K) * 4) + (size_t)a.nw * round256((size_t)(a.M * a.N) * 4);
+}
+
+// Device address of p when it is page-locked host memory mapped for the
+// current device; nullptr otherwise (pageable or device memory).
+template <class T>
+T* mapped_host(T* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer || !at.hostPointer) return nullptr;
+    const ptrdiff_t off = reinterpret_cast<const char*>(p) - static_cast<const char*>(at.hostPointer);
+    return reinterpret_cast<T*>(static_cast<char*>(at.devicePointer) + off);
+}
+
+// A GEMV whose x and outputs are host buffers: returns once the outputs hold
+// the result. Zero-copy route when every buffer is mapped page-locked memory
+// and every slice runs on the register-resident-x kernel: x is fetched into
+// the workspace by a kernel (fetch_host_launch), the GEMV follows as its
+// programmatic dependent and stores its outputs straight into host memory.
+// Otherwise one cudaMemcpyAsync per buffer through the workspace around an
+// ordinary call.
+int run_gemv_host(const GemvArgs& a, void* ws, size_t ws_bytes, qg_stream_t stream) {
+    int rc = validate_gemv(a);
+    if (rc) return rc;
+    if (ws && !aligned(ws, 16)) return QG_ERR_MISALIGNED;
+    const DevCtx* dc = nullptr;
+    rc = current_ctx(&dc);
+    if (rc) return rc;
+    const size_t stage = host_stage_bytes(a);
+    if (!ws || ws_bytes < stage) return QG_ERR_WORKSPACE;
+    // The staging area sits at the end of the workspace; the call keeps the
+    // part before it.
+    const size_t off = (ws_bytes - stage) & ~(size_t)255;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    float* xs = reinterpret_cast<float*>(base + off);
+    float* ys[2];
+    ys[0] = reinterpret_cast<float*>(base + off + round256((size_t)(a.M * a.K) * 4));
+    ys[1] = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ys[0]) +
+                                     round256((size_t)(a.M * a.N) * 4));
+    void* call_ws = off ? ws : nullptr;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t xb = (size_t)(a.M * a.K) * 4, yb = (size_t)(a.M * a.N) * 4;
+
+    GemvArgs d = a;
+    d.x = xs;
+    d.isolated = true;  // the call is waited for before it returns
+    float* ym[2] = {nullptr, nullptr};
+    bool direct = mapped_host(a.x) != nullptr && aligned(a.x, 16);
+    for (int i = 0; i < a.nw && direct; ++i) {
+        ym[i] = mapped_host(a.y[i]);
+        direct = ym[i] != nullptr;
+    }
+    if (direct) {
+        GemvArgs t = d;
+        t.y[0] = ym[0];
+        t.y[1] = ym[1];
+        direct = !prefill_eligible(*dc, t) &&
+                 !(quant_prefill_eligible(*dc, t) && off >= quant_prefill_workspace_bytes(t)) &&
+                 gemv_xreg_only(*dc, t);
+        if (direct) d = t;
+    }
+    if (direct) {
+        rc = fetch_host_launch(*dc, mapped_host(a.x), xs, a.M * a.K, s);
+        if (rc) return rc;
+        d.x_from_prev = true;
+        rc = gemv_launch(*dc, d, nullptr, 0, s);
+        if (rc) return rc;
+    } else {
+        d.y[0] = ys[0];
+        d.y[1] = ys[1];
+        // The call's own workspace need, checked before anything is enqueued
+        // (run_gemv's rule: the tensor-core prefill when its workspace fits,
+        // else the CUDA-core kernels).
+        size_t need = gemv_workspace_bytes(*dc, d);
+        if (prefill_eligible(*dc, d))
+            need = prefill_workspace_bytes(d);
+        else if (quant_prefill_eligible(*dc, d) && off >= quant_prefill_workspace_bytes(d))
+            need = 0;  // the tensor-core prefill, whose workspace fits
+        if (need > off) return QG_ERR_WORKSPACE;
+        cudaError_t e = cudaMemcpyAsync(xs, a.x, xb, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        rc = run_gemv(d, call_ws, off, stream);
+        if (rc) return rc;
+        for (int i = 0; i < a.nw; ++i) {
+            e = cudaMemcpyAsync(a.y[i], ys[i], yb, cudaMemcpyDeviceToHost, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+    }
+    const cudaError_t e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 int q4_k_cuda_core(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
@@ -209,6 +310,7 @@ int workspace_size_impl(int op, int64_t M, int64_t N, int64_t K, int group_size,
     switch (op) {
         case QG_OP_Q4_0: a.fmt = FMT_Q4_0; a.nw = 1; break;
         case QG_OP_DUAL_Q4_0: a.fmt = FMT_Q4_0; a.nw = 2; break;
+        case QG_OP_DUAL_Q4_0_HOST: a.fmt = FMT_Q4_0; a.nw = 2; break;
         case QG_OP_Q4_K: a.fmt = FMT_Q4_K; a.nw = 1; break;
         case QG_OP_AFFINE:
             if (packed != 0 && packed != 1) return QG_ERR_INVALID_ARG;
@@ -233,6 +335,7 @@ int workspace_size_impl(int op, int64_t M, int64_t N, int64_t K, int group_size,
     if (prefill_eligible(*dc, a)) *bytes = std::max(*bytes, prefill_workspace_bytes(a));
     if (quant_prefill && quant_prefill_eligible(*dc, a))
         *bytes = std::max(*bytes, quant_prefill_workspace_bytes(a));
+    if (op == QG_OP_DUAL_Q4_0_HOST) *bytes = host_stage_offset(*bytes) + host_stage_bytes(a);
     return QG_OK;
 }
 
@@ -271,6 +374,21 @@ int qgemv_dual_q4_0(const void* w_a, const void* w_b, const float* x, float* y_a
     a.x = x;
     a.M = M; a.N = N; a.K = K;
     return run_gemv(a, workspace, workspace_bytes, stream);
+}
+
+int qgemv_dual_q4_0_host(const void* w_a, const void* w_b, const float* x, float* y_a,
+                         float* y_b, int64_t M, int64_t N, int64_t K, void* workspace,
+                         size_t workspace_bytes, qg_stream_t stream) {
+    GemvArgs a{};
+    a.fmt = FMT_Q4_0;
+    a.nw = 2;
+    a.w[0] = static_cast<const uint8_t*>(w_a);
+    a.w[1] = static_cast<const uint8_t*>(w_b);
+    a.y[0] = y_a;
+    a.y[1] = y_b;
+    a.x = x;
+    a.M = M; a.N = N; a.K = K;
+    return run_gemv_host(a, workspace, workspace_bytes, stream);
 }
 
 int qgemv_q4_k(const void* w, const float* x, float* y, int64_t M, int64_t N, int64_t K,
@@ -452,10 +570,9 @@ int qg_set_option(int option, int64_t value) {
             g_opt_xreg_ahead.store(value, std::memory_order_relaxed);
             return QG_OK;
         case QG_OPT_XREG_WARPS:
-            if (value != 0 && value != 4) return QG_ERR_INVALID_ARG;
+            if (value != 0 && value != 4 && value != 8 && value != 16) return QG_ERR_INVALID_ARG;
             g_opt_xreg_warps.store(value, std::memory_order_relaxed);
-            return QG_OK;
-        case QG_OPT_XREG_CTAS:
+            return QG_OK;        case QG_OPT_XREG_CTAS:
             if (value < 1 || value > 4) return QG_ERR_INVALID_ARG;
             g_opt_xreg_ctas.store(value, std::memory_order_relaxed);
             return QG_OK;

@@ -166,10 +166,25 @@ struct GemvArgs {
     const float* biases;       // affine only
     int64_t M, N, K;
     int gs;                    // affine only
+    // x is written by the kernel launched just before on the stream: the
+    // register-resident-x kernel is then launched as its programmatic
+    // dependent and waits for it before reading x, whatever QG_OPT_PDL says.
+    bool x_from_prev;
+    // The call runs alone: the caller waits for it before anything else is
+    // queued. The register-resident-x kernel then gives its CTA all of the
+    // SM's shared memory (no room is kept for the next call's CTAs) and never
+    // takes the four-warp shape meant for overlapping calls.
+    bool isolated;
 };
 
 size_t gemv_workspace_bytes(const DevCtx& dc, const GemvArgs& a);
 int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, cudaStream_t s);
+bool gemv_xreg_only(const DevCtx& dc, const GemvArgs& a);
+
+// dst[0..n) = src[0..n) (f32) by a kernel; src is mapped host memory, n a
+// multiple of 4, both pointers 16-byte aligned (host_io.cu).
+int fetch_host_launch(const DevCtx& dc, const float* src, float* dst, long long n,
+                      cudaStream_t s);
 
 // The prepared AF4-g64 layout: repack from codes and bf16 scale / bias bits
 // (af4.cu), and the qmm that reads it, M <= 32 (af4_gemv.cu).

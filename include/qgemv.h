@@ -87,7 +87,9 @@ enum {
     QG_OP_DUAL_Q4_0 = 1,
     QG_OP_Q4_K = 2,
     QG_OP_AFFINE = 3,
-    QG_OP_AF4_G64 = 4
+    QG_OP_AF4_G64 = 4,
+    QG_OP_DUAL_Q4_0_HOST = 5  /* qgemv_dual_q4_0_host: the call's own workspace plus
+                                 device staging for x, y_a, y_b */
 };
 
 /* Single Q4_0 projection: y[M,N] = x[M,K] . dequant(w)[N,K]^T.
@@ -118,6 +120,33 @@ QG_API int qgemv_q4_0(const void* w, const float* x, float* y, int64_t M, int64_
 QG_API int qgemv_dual_q4_0(const void* w_a, const void* w_b, const float* x, float* y_a, float* y_b,
                     int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                     qg_stream_t stream);
+
+/* qgemv_dual_q4_0 with x, y_a and y_b in HOST memory; w_a and w_b stay in
+ * device memory (model weights are resident). The operation is the page's
+ * (fused_dual_proj_q4_0.rs, dispatch_fused_dual_proj_q4_0); taking host
+ * buffers and returning only when the result is in them is this library's
+ * own addition, for callers whose input arrives from, and whose output goes
+ * back to, the host every step (the host round trip qkv_split.rs's module
+ * doc names as the cost to cut).
+ * - Synchronous: returns after y_a and y_b hold the result (it synchronizes
+ *   `stream`, so work queued on it earlier completes first). Results equal
+ *   qgemv_dual_q4_0's on device copies of the same buffers, bit for bit.
+ * - Zero-copy: when x, y_a and y_b are page-locked host memory mapped for the
+ *   device (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped),
+ *   x is 16-byte aligned, and every slice of the call runs on the
+ *   register-resident-x kernel (M <= 2 for this format), the kernel reads x
+ *   and writes y_a, y_b in host memory directly (plain loads and stores over
+ *   the host link); nothing else is enqueued and no workspace is used.
+ * - Otherwise (pageable buffers, other M): x is copied into the workspace,
+ *   the call runs there and y_a, y_b are copied back, each with one
+ *   cudaMemcpyAsync on `stream`. workspace: device memory of at least
+ *   qg_workspace_size(QG_OP_DUAL_Q4_0_HOST, M, N, K, 0, 0) bytes, 16-byte
+ *   aligned; QG_ERR_WORKSPACE (nothing enqueued) when it is smaller.
+ * - Host buffers must not overlap one another. Errors as for
+ *   qgemv_dual_q4_0; a failed copy or synchronization returns QG_ERR_CUDA. */
+QG_API int qgemv_dual_q4_0_host(const void* w_a, const void* w_b, const float* x, float* y_a,
+                                float* y_b, int64_t M, int64_t N, int64_t K, void* workspace,
+                                size_t workspace_bytes, qg_stream_t stream);
 
 /* Q4_K GEMV. Page: q4_k_gemv_v2.rs (ferrum-kernels 0.7.7),
  * dispatch_gemv_q4k_v2_offset (M = 1 there; any M here; the two paths of
@@ -297,11 +326,15 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * QG_OPT_XREG_AHEAD (default 0 = every slot of the ring; else 1..16): chunks
  * of weights the register-resident-x kernel keeps in flight at most (tuning).
  *
- * QG_OPT_XREG_WARPS (default 0 = automatic; or 4) and QG_OPT_XREG_CTAS
- * (default 1; 1..4): consumer warps per CTA and CTAs per SM per call of the
- * register-resident-x kernel (tuning; results are bitwise the same). With
- * four consumer warps (rows of at most 4096 weights of K), four CTAs share an
- * SM; automatic picks them when QG_OPT_PDL is 2, eight warps otherwise. */
+ * QG_OPT_XREG_WARPS (default 0 = automatic; or 4, 8, 16) and
+ * QG_OPT_XREG_CTAS (default 1; 1..4): consumer warps per CTA and CTAs per SM
+ * per call of the register-resident-x kernel (tuning; results are bitwise
+ * the same). A count that does not suit the shape (the warps of one row
+ * group must divide it; sixteen warps take one x row) falls back to
+ * automatic. With four consumer warps (rows of at most 4096 weights of K),
+ * four CTAs share an SM; automatic picks them when QG_OPT_PDL is 2, eight
+ * warps otherwise and for the host-buffer call (a lone call, which also
+ * takes all of the SM's shared memory). */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
        QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6, QG_OPT_STAGED_WARPS = 7,
        QG_OPT_PREFILL_FOLD = 8, QG_OPT_XREG = 9, QG_OPT_XREG_AHEAD = 10,

@@ -227,11 +227,14 @@ def test_xreg_independent_calls_mode():
     assert qg.device_error() == 0
 
 
-@pytest.fixture(params=["8 warps", "4 warps"])
+@pytest.fixture(params=["automatic", "4 warps", "8 warps", "16 warps"])
 def cta_shape(request):
-    """The kernel's two CTA shapes: eight consumer warps (two CTAs per SM) and
-    four (four CTAs per SM, taken automatically for independent calls)."""
-    qg.set_option(qg.QG_OPT_XREG_WARPS, 4 if request.param == "4 warps" else 0)
+    """The kernel's CTA shapes: automatic (eight consumer warps here, two CTAs
+    per SM), four (four CTAs per SM, taken automatically for independent
+    calls), eight, and sixteen (one CTA per SM). A count the shape does not
+    allow falls back to automatic."""
+    w = {"automatic": 0, "4 warps": 4, "8 warps": 8, "16 warps": 16}[request.param]
+    qg.set_option(qg.QG_OPT_XREG_WARPS, w)
     yield request.param
     qg.set_option(qg.QG_OPT_XREG_WARPS, 0)
 
@@ -264,19 +267,20 @@ def test_xreg_cta_shapes_q4_k_and_affine(M, cta_shape):
 
 
 def test_xreg_cta_shape_does_not_change_results():
-    """Each output's arithmetic depends on the format, M, K and x only: the
-    two CTA shapes give bitwise the same y."""
+    """Each output's arithmetic depends on the format, M, K and x only: every
+    CTA shape gives bitwise the same y."""
     N, K = 777, 4096
     c = synth.q4_0_case(6300, N, K, 1, dual=True)
     wa, wb, x = to_dev(c["w"]), to_dev(c["w_b"]), to_dev(c["x"])
     base = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
-    qg.set_option(qg.QG_OPT_XREG_WARPS, 4)
     try:
-        for ctas in (1, 2, 4):
-            qg.set_option(qg.QG_OPT_XREG_CTAS, ctas)
-            ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
-            assert_bitwise(ya, base[0], f"4 warps, {ctas} CTAs per SM, y_a")
-            assert_bitwise(yb, base[1], f"4 warps, {ctas} CTAs per SM, y_b")
+        for warps in (4, 8, 16):
+            qg.set_option(qg.QG_OPT_XREG_WARPS, warps)
+            for ctas in (1, 2, 4):
+                qg.set_option(qg.QG_OPT_XREG_CTAS, ctas)
+                ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
+                assert_bitwise(ya, base[0], f"{warps} warps, {ctas} CTAs per SM, y_a")
+                assert_bitwise(yb, base[1], f"{warps} warps, {ctas} CTAs per SM, y_b")
     finally:
         qg.set_option(qg.QG_OPT_XREG_WARPS, 0)
         qg.set_option(qg.QG_OPT_XREG_CTAS, 1)
