@@ -378,6 +378,12 @@ int rows_blocks_per_cta(long long N) { return (N / 64) % 2 == 0 ? 2 : 1; }
 
 int af4_gemv_launch(const DevCtx& dc, const float* x, const uint32_t* plane, const uint32_t* meta,
                     float* y, long long M, long long N, long long K, cudaStream_t s) {
+    // One or two rows of x: the register-resident-x kernel when it takes the
+    // shape (for both M or for neither).
+    if (M <= 2) {
+        const int rc = af4_xreg_launch(dc, x, plane, meta, y, M, N, K, s);
+        if (rc != QG_ERR_UNSUPPORTED) return rc;
+    }
     Params p{};
     p.x = x;
     p.plane = reinterpret_cast<const uint4*>(plane);

@@ -55,6 +55,7 @@
 
 #include <cuda_fp16.h>
 
+#include "prefill_common.cuh"
 #include "qg_internal.cuh"
 
 namespace qg {
@@ -69,7 +70,9 @@ struct Params {
     int M, N, K, nw;
     int log2gs, G;
     int row_bytes;             // code bytes of one weight row
-    int rows_base, rows_rem;   // CTA c takes rows_base rows, one more when c < rows_rem
+    int rows_base, rows_rem;   // CTA c takes rows_base units of rows, one more when c < rows_rem
+    int row_unit;              // rows per unit (0 or 1: single rows; AF4: 4, so chunks start
+                               // on 4-row boundaries as its metadata copies require)
     int S, slot_bytes;         // ring slots and their size
     int sb_off;                // offset of the chunk's scales in a slot (biases follow)
     int WG, NRG, RC;           // warps per row group, row groups, rows per chunk
@@ -121,6 +124,12 @@ __host__ __device__ constexpr Loc q4k_loc(int k) {
 __host__ __device__ constexpr Loc packed_loc(int k) { return Loc{k >> 2, 2 * (k & 3), 2 * (k & 3) + 1}; }
 // u8 affine unit (32 bytes): element e = byte e % 4 of word e / 4.
 __host__ __device__ constexpr Loc u8_loc(int k) { return Loc{k >> 1, 2 * (k & 1), 2 * (k & 1) + 1}; }
+// AF4-g64 unit (16 bytes, one 32-group of a row): word c holds, for p = 0..3,
+// the element pair (16 (p >> 1) + 4c + 2 (p & 1), +1) in nibbles p and 4 + p.
+// Pair k = elements (2k, 2k+1): c = (k & 7) >> 1, p = 2 (k >> 3) + (k & 1).
+__host__ __device__ constexpr Loc af4_loc(int k) {
+    return Loc{(k & 7) >> 1, 2 * (k >> 3) + (k & 1), 4 + 2 * (k >> 3) + (k & 1)};
+}
 
 // log2 of the power of two each decoded element of pair k carries (removed
 // from x when x is loaded).
@@ -129,6 +138,7 @@ __host__ __device__ constexpr int shift_a(int k) {
     return FMT == FMT_AFF_U8       ? 0
            : FMT == FMT_Q4_0       ? nib_shift(q40_loc(PAR, k).pa)
            : FMT == FMT_Q4_K       ? nib_shift(q4k_loc(k).pa)
+           : FMT == FMT_AF4        ? nib_shift(af4_loc(k).pa)
                                    : nib_shift(packed_loc(k).pa);
 }
 template <int FMT, int PAR>
@@ -136,6 +146,7 @@ __host__ __device__ constexpr int shift_b(int k) {
     return FMT == FMT_AFF_U8       ? 0
            : FMT == FMT_Q4_0       ? nib_shift(q40_loc(PAR, k).pb)
            : FMT == FMT_Q4_K       ? nib_shift(q4k_loc(k).pb)
+           : FMT == FMT_AF4        ? nib_shift(af4_loc(k).pb)
                                    : nib_shift(packed_loc(k).pb);
 }
 
@@ -150,7 +161,10 @@ __device__ __forceinline__ float2 pair(const uint32_t (&wd)[NWD], int k) {
         const Loc L = u8_loc(k);
         return make_float2(byte_f(wd[L.word], L.pa), byte_f(wd[L.word], L.pb));
     }
-    const Loc L = FMT == FMT_Q4_0 ? q40_loc(PAR, k) : FMT == FMT_Q4_K ? q4k_loc(k) : packed_loc(k);
+    const Loc L = FMT == FMT_Q4_0   ? q40_loc(PAR, k)
+                  : FMT == FMT_Q4_K ? q4k_loc(k)
+                  : FMT == FMT_AF4  ? af4_loc(k)
+                                    : packed_loc(k);
     return make_float2(nib(wd[L.word], L.pa), nib(wd[L.word], L.pb));
 }
 
@@ -195,6 +209,27 @@ __device__ __forceinline__ Chunk chunk_at(int r, int re, int N, int RC) {
     const int wi = r >= N ? 1 : 0;
     const int row0 = r - wi * N;
     return Chunk{wi, row0, min(min(re - r, RC), N - row0)};
+}
+// AF4: a chunk also stays inside its 64-row block (one copy per block).
+template <int FMT>
+__device__ __forceinline__ Chunk chunk_of(int r, int re, int N, int RC) {
+    if (FMT == FMT_AF4) return Chunk{0, r, min(min(re - r, RC), 64 - (r & 63))};
+    return chunk_at(r, re, N, RC);
+}
+
+// The CTA's row range [rb, re).
+__device__ __forceinline__ void cta_rows(const Params& p, int& rb, int& re) {
+    const int cta = blockIdx.x, ru = max(1, p.row_unit);
+    rb = ru * (cta * p.rows_base + min(cta, p.rows_rem));
+    re = rb + ru * (p.rows_base + (cta < p.rows_rem ? 1 : 0));
+}
+
+// L2 prefetch of a 2-D tensor-map box (no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 
 // All consumer threads load x with coalesced 16-byte loads into shared memory,
@@ -361,10 +396,12 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc0[m] = make_float2(FMT == FMT_Q4_0 ? xoff[m] : 0.0f, 0.0f);
     const float2 zero2 = make_float2(0.0f, 0.0f);
-    const int cta = blockIdx.x;
-    const int rb = cta * p.rows_base + min(cta, p.rows_rem);
-    const int re = rb + p.rows_base + (cta < p.rows_rem ? 1 : 0);
+    int rb, re;
+    cta_rows(p, rb, re);
     const int nthr = p.NRG * p.WG * 32, tid = warp * 32 + lane;
+    // AF4: the 16-byte chunk of row rr of this lane's unit sits at rr ^ swz in
+    // the unit's line of the slot (the copy's 64- or 128-byte swizzle).
+    const int af4_swz = p.RC == 8 ? (uu & 7) : ((uu >> 1) & 3);
     const int NRG = p.NRG, RC = p.RC, WG = p.WG, N = p.N;
     const size_t row_bytes = (size_t)p.row_bytes;
     // Per-warp partial sums of the CTA's rows wait in red[row - fb][m][gw]
@@ -391,7 +428,7 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
     int slot = 0;
     uint32_t phase = 0;
     for (int r = rb; r < re;) {
-        const Chunk ch = chunk_at(r, re, N, RC);
+        const Chunk ch = chunk_of<FMT>(r, re, N, RC);
         if (r + ch.n - fb > p.rbuf) flush(r, false);
         if (!dead && !mbar_wait(smem_addr(&full[slot]), phase)) {
             report_error(p.err, DEVERR_WAIT_FULL);
@@ -455,6 +492,28 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
                     const float tot = mine + __shfl_xor_sync(0xffffffffu, send, 1);
                     o[m] = __fmaf_rn(a, tot, -(bm * xoff[m]));
                 }
+            } else if constexpr (FMT == FMT_AF4) {
+                const uint4 q0 = *reinterpret_cast<const uint4*>(
+                    base + ((size_t)uu * RC + (rr ^ af4_swz)) * 16);
+                const uint32_t wd[4] = {q0.x, q0.y, q0.z, q0.w};
+                // bf16 scale | bf16 bias << 16 of the unit's 64-group.
+                const uint32_t mw = *reinterpret_cast<const uint32_t*>(
+                    base + p.sb_off + ((size_t)(uu >> 1) * RC + rr) * 4);
+                const float sc = __uint_as_float(mw << 16);
+                const float bi = __uint_as_float(mw & 0xFFFF0000u);
+                float2 acc[MT][2];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float2 f = pair<FMT, 0, 4>(wd, k);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        acc[m][k & 1] = __ffma2_rn(f, X[m][k], k < 2 ? zero2 : acc[m][k & 1]);
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float2 t = __fadd2_rn(acc[m][0], acc[m][1]);
+                    o[m] = __fmaf_rn(sc, t.x + t.y, bi * xoff[m]);
+                }
             } else {
                 constexpr int NWD = FMT == FMT_AFF_U8 ? 8 : 4;
                 uint32_t wd[NWD];
@@ -514,16 +573,16 @@ __device__ __forceinline__ void consume(const Params& p, uint8_t* ring, uint64_t
     flush(re, true);
 }
 
+// The kernel. mq / mm: AF4's tensor maps of the plane and the metadata
+// (null for the other formats).
 template <int FMT, int MT, int NWC, int RPG>
-__global__ void __launch_bounds__((NWC + 1) * 32,
-                                  MT == 4   ? 1
-                                  : NWC == 4 ? (MT == 1 ? 4 : 3)
-                                  : ((NWC == 8 || NWC == 12) && MT == 1) ? 2
-                                             : 1)
-    gemv_xreg_kernel(const Params p) {
+__device__ __forceinline__ void xreg_body(const Params& p, const CUtensorMap* mq,
+                                          const CUtensorMap* mm) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.S * p.slot_bytes);
+    // AF4's swizzled copies need their slots on 1024-byte boundaries (the
+    // launch adds 1024 bytes for this).
+    uint8_t* ring = FMT == FMT_AF4 ? smem + ((1024u - (smem_addr(smem) & 1023u)) & 1023u) : smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)p.S * p.slot_bytes);
     uint64_t* empty = full + p.S;
     float* red = reinterpret_cast<float*>(empty + p.S);
     float* xst = red + (size_t)p.red_floats;  // 16-byte aligned (red_floats % 4 == 0)
@@ -531,9 +590,8 @@ __global__ void __launch_bounds__((NWC + 1) * 32,
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int cta = blockIdx.x;
-    const int rb = cta * p.rows_base + min(cta, p.rows_rem);
-    const int re = rb + p.rows_base + (cta < p.rows_rem ? 1 : 0);
+    int rb, re;
+    cta_rows(p, rb, re);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.S; ++i) {
@@ -563,7 +621,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32,
         bool ok = true, prefetched = false;
         int i = 0;
         for (int r = rb; r < re; ++i) {
-            const Chunk ch = chunk_at(r, re, p.N, p.RC);
+            const Chunk ch = chunk_of<FMT>(r, re, p.N, p.RC);
             r += ch.n;
             const int slot = i % p.S, use = i / p.S;
             if (use > 0 && !mbar_wait(smem_addr(&empty[slot]), (use - 1) & 1)) {
@@ -583,6 +641,19 @@ __global__ void __launch_bounds__((NWC + 1) * 32,
             }
             uint8_t* dst = ring + (size_t)slot * p.slot_bytes;
             const uint32_t bar = smem_addr(&full[slot]);
+            if constexpr (FMT == FMT_AF4) {
+                // RC rows of the chunk's 64-row block, all 32-groups (codes)
+                // and 64-groups (metadata): two tensor copies of fixed size
+                // (rows past the block's end read as zeros, unused ones are
+                // never stored).
+                const uint32_t qb = (uint32_t)(p.RC * 16 * p.units);
+                const uint32_t mb = (uint32_t)(p.RC * 4 * (p.units >> 1));
+                mbar_arrive_expect_tx(bar, qb + mb);
+                prefill::tma_load_2d(smem_addr(dst), mq, (ch.row0 & 63) * 16,
+                                     (ch.row0 >> 6) * p.units, bar);
+                prefill::tma_load_2d(smem_addr(dst + p.sb_off), mm, (ch.row0 & 63) * 4,
+                                     (ch.row0 >> 6) * (p.units >> 1), bar);
+            } else {
             const uint32_t qb = (uint32_t)(ch.n * p.row_bytes);
             const uint32_t sbb = kAffine ? (uint32_t)(ch.n * p.G * 4) : 0u;
             mbar_arrive_expect_tx(bar, qb + 2u * sbb);
@@ -592,6 +663,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32,
                 bulk_g2s(smem_addr(dst + p.sb_off), p.s + go, sbb, bar, pol);
                 bulk_g2s(smem_addr(dst + p.sb_off + p.RC * p.G * 4), p.b + go, sbb, bar, pol);
             }
+            }
             issued = i + 1;
             if (i == p.S - 1 || r == re) {
                 if (!prefetched && r < re && p.ahead == 0) {
@@ -599,8 +671,13 @@ __global__ void __launch_bounds__((NWC + 1) * 32,
                     // bring it from HBM into L2 now, so that the ring is later
                     // refilled at L2 latency.
                     for (int r2 = r; r2 < re;) {
-                        const Chunk c2 = chunk_at(r2, re, p.N, p.RC);
+                        const Chunk c2 = chunk_of<FMT>(r2, re, p.N, p.RC);
                         r2 += c2.n;
+                        if constexpr (FMT == FMT_AF4) {
+                            tma_prefetch_2d(mq, (c2.row0 & 63) * 16, (c2.row0 >> 6) * p.units);
+                            tma_prefetch_2d(mm, (c2.row0 & 63) * 4, (c2.row0 >> 6) * (p.units >> 1));
+                            continue;
+                        }
                         bulk_prefetch_l2(p.w[c2.wi] + (long long)c2.row0 * p.row_bytes,
                                          (uint32_t)(c2.n * p.row_bytes));
                         if (kAffine) {
@@ -636,6 +713,26 @@ __global__ void __launch_bounds__((NWC + 1) * 32,
         consume<FMT, MT, NWC, RPG, 0>(p, ring, full, empty, red, xst, xmax, warp, lane);
     }
 }
+
+#define QG_XREG_BOUNDS                                                      \
+    __launch_bounds__((NWC + 1) * 32, MT == 4    ? 1                        \
+                                      : NWC == 4 ? (MT == 1 ? 4 : 3)        \
+                                      : ((NWC == 8 || NWC == 12) && MT == 1) ? 2 \
+                                                                             : 1)
+
+template <int FMT, int MT, int NWC, int RPG>
+__global__ void QG_XREG_BOUNDS gemv_xreg_kernel(const Params p) {
+    xreg_body<FMT, MT, NWC, RPG>(p, nullptr, nullptr);
+}
+
+// AF4-g64: the same kernel with the tensor maps of the prepared layout.
+template <int MT, int NWC, int RPG>
+__global__ void QG_XREG_BOUNDS gemv_xreg_af4_kernel(const Params p,
+                                                    const __grid_constant__ CUtensorMap mq,
+                                                    const __grid_constant__ CUtensorMap mm) {
+    xreg_body<FMT_AF4, MT, NWC, RPG>(p, &mq, &mm);
+}
+#undef QG_XREG_BOUNDS
 
 template <int FMT, int MT, int NWC, int RPG>
 int launch(const DevCtx& dc, const Params& kp, int grid, int smem, bool pdl, cudaStream_t s) {

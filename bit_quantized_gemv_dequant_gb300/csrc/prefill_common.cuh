@@ -171,5 +171,8 @@ int launch_fold_kernel(const DevCtx& dc, bool packed, bool gs16, const CUtensorM
                        const CUtensorMap& mx, const FoldParams& fp, dim3 grid, cudaStream_t s);
 int fold_smem_bytes(bool packed);
 
+// cuTensorMapEncodeTiled from the driver, looked up once (prefill.cu).
+int encoder(PFN_cuTensorMapEncodeTiled_v12000* out);
+
 }  // namespace prefill
 }  // namespace qg

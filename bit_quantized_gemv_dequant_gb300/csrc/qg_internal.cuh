@@ -154,7 +154,9 @@ long long launch_option(int option);
 
 // ----------------------------------------------------------------- launchers
 // GEMV family (gemv.cu). fmt: see GemvFmt. Returns a qg_status.
-enum GemvFmt : int { FMT_Q4_0 = 0, FMT_Q4_K = 1, FMT_AFF_U8 = 2, FMT_AFF_PACKED = 3 };
+// FMT_AF4: the prepared AF4-g64 layout (qmm_af4_g64); only the
+// register-resident-x kernel reads it through GemvFmt.
+enum GemvFmt : int { FMT_Q4_0 = 0, FMT_Q4_K = 1, FMT_AFF_U8 = 2, FMT_AFF_PACKED = 3, FMT_AF4 = 4 };
 
 struct GemvArgs {
     int fmt;
@@ -192,6 +194,11 @@ int af4_prepare_launch(const DevCtx& dc, const uint8_t* codes, const uint16_t* s
                        const uint16_t* bb, uint32_t* plane, uint32_t* meta, long long N,
                        long long K, cudaStream_t s);
 int af4_gemv_launch(const DevCtx& dc, const float* x, const uint32_t* plane, const uint32_t* meta,
+                    float* y, long long M, long long N, long long K, cudaStream_t s);
+// qmm_af4_g64 on the register-resident-x kernel for M <= 2 (gemv_xreg_af4.cu);
+// QG_ERR_UNSUPPORTED, with nothing enqueued, when the shape or alignment does
+// not suit it.
+int af4_xreg_launch(const DevCtx& dc, const float* x, const uint32_t* plane, const uint32_t* meta,
                     float* y, long long M, long long N, long long K, cudaStream_t s);
 
 // Affine prefill on the tensor cores (prefill.cu). Eligibility depends on the

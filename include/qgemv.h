@@ -236,10 +236,14 @@ QG_API int dequant_affine(const void* q, const float* scales, const float* biase
  *
  * qmm_af4_g64: y[M,N] = x[M,K] . w[N,K]^T from the prepared layout, M <= 32
  * (the page's limit). The page's kernel rounds x to bf16 (error class:
- * relative RMS and max |err| / max(|y|, 1) <= 5e-3). Here the kernel reads
- * the prepared words directly and computes in f32 on the CUDA cores for
- * every M: |y - exact| <= 1e-5 * sum_k |x w| + 1e-6. Row m of y is bitwise
- * the same for every M in 1..8, and for every M in 9..32. x and y 4-byte aligned, plane 16-byte aligned,
+ * relative RMS and max |err| / max(|y|, 1) <= 5e-3). Here the kernels read
+ * the prepared words directly and compute in f32 on the CUDA cores for
+ * every M: |y - exact| <= 1e-5 * sum_k |x w| + 1e-6. M = 1 and 2 take the
+ * register-resident-x kernel when K <= 4096 (K <= 1024, 2048 or 4096 of
+ * whole warps of 32-groups: K in (2048, 3072] excluded) and x, plane and
+ * metadata are 16-byte aligned; other calls a kernel that splits K across a
+ * thread-block cluster. Row m of y is bitwise the same for M = 1 and 2, for
+ * every M in 3..8 and for every M in 9..32. x and y 4-byte aligned, plane 16-byte aligned,
  * metadata 4-byte aligned; y must not overlap an input. No workspace
  * (qg_workspace_size reports 0; workspace may be NULL). */
 QG_API int qg_prepare_af4_g64(const uint8_t* codes, const uint16_t* scales_bf16,

@@ -9,8 +9,10 @@ biases taken exactly as f32, under the f32 bar (1e-5 * sum |x w| + 1e-6) for
 every M. Shapes cover one and two row blocks per CTA (odd and even N / 64),
 one and several K slices per row block (a cluster of 1 to 8 CTAs), x staged
 in more than one sub-slice (M = 32, K = 12288), odd group counts, every M
-tile (8, 4, 2, 1) and the 4096 x 4096 workload the benchmark times. Row m
-of y must not depend on M within M <= 8 and within M > 8, and x at a 4-byte
+tile (8, 4, 2, 1) and the 4096 x 4096 workload the benchmark times; for M <= 2 and
+K <= 4096 the register-resident-x kernel (agreement with the cluster kernel,
+every launch mode, metadata off a 16-byte boundary falling back). Row m of y
+must not depend on M within M in 1..2, 3..8 and 9..32, and x at a 4-byte
 offset (the scalar staging path) must give bitwise the same y.
 """
 import numpy as np
@@ -57,8 +59,9 @@ def test_qmm_af4_parity(M, N, K):
 
 @pytest.mark.parametrize("N,K", [(192, 512), (64, 12288), (512, 4096)])
 def test_qmm_af4_rows_do_not_depend_on_m(N, K):
-    """The K slicing is one for M <= 8 and one for M > 8; within each class
-    row m of y is bitwise the same whatever M is."""
+    """Within each class of M (1..2 on the register-resident-x kernel when it
+    takes the shape, 3..8 and 9..32 with one K slicing each) row m of y is
+    bitwise the same whatever M is."""
     c = synth.af4_case(7200 + N, N, K, 32)
     plane, meta = _prepare(c)
     x = to_dev(c["x"])
@@ -67,9 +70,12 @@ def test_qmm_af4_rows_do_not_depend_on_m(N, K):
         yM = qg.qmm_af4_g64(x[32 - M:].contiguous(), plane, meta, N)
         assert_bitwise(yM, y32[32 - M:], f"af4 rows of M={M} vs M=32")
     y8 = qg.qmm_af4_g64(x[:8].contiguous(), plane, meta, N)
-    for M in (1, 3, 5):
+    for M in (3, 5):
         yM = qg.qmm_af4_g64(x[8 - M:8].contiguous(), plane, meta, N)
         assert_bitwise(yM, y8[8 - M:], f"af4 rows of M={M} vs M=8")
+    y2 = qg.qmm_af4_g64(x[:2].contiguous(), plane, meta, N)
+    y1 = qg.qmm_af4_g64(x[1:2].contiguous(), plane, meta, N)
+    assert_bitwise(y1, y2[1:], "af4 rows of M=1 vs M=2")
 
 
 def test_qmm_af4_unaligned_x_is_bitwise_equal():
@@ -138,3 +144,65 @@ def test_qmm_af4_validation():
     with pytest.raises(qg.QGError):
         qg.prepare_af4_g64(to_dev(c["q"][:, :96].copy()), _bf16(c["s_bits"][:, :1].copy()),
                            _bf16(c["b_bits"][:, :1].copy()))   # K % 64 != 0
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("N,K", [(192, 512), (128, 1088), (256, 4096), (64, 64)])
+def test_qmm_af4_register_path_agrees_with_cluster_kernel(M, N, K):
+    """With one or two rows of x (K <= 4096, 16-byte aligned buffers) the
+    register-resident-x kernel takes the call; with QG_OPT_XREG = 0 the
+    cluster kernel does. Both are within the bound of the exact value, so
+    within twice of each other."""
+    c = synth.af4_case(7500 + M + N + K, N, K, M)
+    plane, meta = _prepare(c)
+    x = to_dev(c["x"])
+    y_new = qg.qmm_af4_g64(x, plane, meta, N)
+    qg.set_option(qg.QG_OPT_XREG, 0)
+    try:
+        y_old = qg.qmm_af4_g64(x, plane, meta, N)
+    finally:
+        qg.set_option(qg.QG_OPT_XREG, 1)
+    ref, bound = oracle.qmm_af4_g64(c["x"], c["q"], c["s_bits"], c["b_bits"], M, N, K)
+    assert_parity(y_new, ref, bound, what=f"af4 register path M={M} N={N} K={K}")
+    assert_parity(y_new, y_old.cpu().numpy().astype(np.float64), bound, rel=2e-5, abs_=2e-6,
+                  what=f"af4 register path vs cluster kernel M={M}")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_qmm_af4_launch_modes(mode):
+    """Every QG_OPT_PDL mode (launch shapes differ): outputs bitwise equal to
+    the default mode's, and a chain whose x is the previous call's y."""
+    N = K = 4096
+    c = synth.af4_case(7600, N, K, 2)
+    plane, meta = _prepare(c)
+    x = to_dev(c["x"])
+    base = qg.qmm_af4_g64(x, plane, meta, N)
+    old = qg.get_option(qg.QG_OPT_PDL)
+    qg.set_option(qg.QG_OPT_PDL, mode)
+    try:
+        y1 = qg.qmm_af4_g64(x, plane, meta, N)
+        y2 = qg.qmm_af4_g64(y1, plane, meta, N) if mode != 2 else None
+        torch.cuda.synchronize()
+    finally:
+        qg.set_option(qg.QG_OPT_PDL, old)
+    assert_bitwise(y1, base, f"PDL mode {mode}")
+    if y2 is not None:
+        ref, bound = oracle.qmm_af4_g64(y1.cpu().numpy(), c["q"], c["s_bits"], c["b_bits"], 2,
+                                        N, K)
+        assert_parity(y2, ref, bound, what=f"chain under PDL mode {mode}")
+    assert qg.device_error() == 0
+
+
+def test_qmm_af4_metadata_off_16_bytes():
+    """Metadata 4 bytes off a 16-byte boundary (allowed) keeps the call on the
+    cluster kernel; results stay within the bar."""
+    M, N, K = 2, 128, 1024
+    c = synth.af4_case(7700, N, K, M)
+    plane, meta = _prepare(c)
+    buf = torch.zeros(meta.numel() + 4, dtype=torch.int32, device=dev())
+    buf[1:1 + meta.numel()] = meta
+    meta_u = buf[1:1 + meta.numel()]
+    assert meta_u.data_ptr() % 16 == 4
+    y = qg.qmm_af4_g64(to_dev(c["x"]), plane, meta_u, N)
+    ref, bound = oracle.qmm_af4_g64(c["x"], c["q"], c["s_bits"], c["b_bits"], M, N, K)
+    assert_parity(y, ref, bound, what="af4 metadata at a 4-byte offset")
