@@ -1,13 +1,15 @@
-// GEMV for one or two input rows with x held in registers, included by one
-// translation unit per weight format.
+// GEMV for one, two or four input rows with x held in registers, included by
+// one translation unit per weight format.
 //
 // Pages: fused_dual_proj_q4_0.rs (mlx-native 0.9.1), q4_k_gemv_v2.rs
 // (ferrum-kernels 0.7.7) and qmm_affine.rs (mlx-native 0.21.1) define the
-// operations; the design below is for sm_103a.
+// operations, the last one also the prepared AF4-g64 layout
+// (prepare_af4_g64); the design below is for sm_103a.
 //
 //  * Lane <-> K unit. Every consumer lane owns one fixed unit of 32 weights
 //    along K (a Q4_0 block; half of a Q4_K 32-byte nibble chunk, i.e. 16
-//    elements of each of two sub-blocks; 32 affine codes) for the whole call.
+//    elements of each of two sub-blocks; 32 affine codes; an AF4 32-group)
+//    for the whole call.
 //    Its 32 x values (per input row) are loaded once, pre-scaled, and stay in
 //    registers; the lane then walks every weight row of its CTA's share. A
 //    row group of WG warps covers one row's K; the NRG = NWC / WG row groups
@@ -30,13 +32,16 @@
 //    chunk half-pair swap one chain each, so each lane ends with the 32-element
 //    chain of one sub-block and applies (d * sc) and -(dmin * m) * sum(x) of
 //    that sub-block (the scale pair it decodes itself, 6-bit fields by PRMT).
-//    Affine: y += s * chain + b * sum(x) per group.
+//    Affine and AF4: y += s * chain + b * sum(x) per group (AF4: bf16 scale
+//    and bias of the unit's 64-group).
 //  * Weights stream into a ring of shared-memory slots, one 1-D TMA bulk copy
 //    per chunk of up to RC consecutive rows of one matrix (plus the chunk's
 //    scales and biases for the affine format), issued by one producer lane
-//    with an evict-first L2 policy and completing on mbarriers. CTAs take
+//    with an evict-first L2 policy and completing on mbarriers. AF4 chunks
+//    (4 or 8 rows of one 64-row block across all of K) are two 2-D tensor
+//    copies instead, the plane's with a 64- or 128-byte swizzle. CTAs take
 //    contiguous, balanced ranges of rows (the dual projection's row list is
-//    W_a then W_b), so the grid is balanced to one row.
+//    W_a then W_b), so the grid is balanced to one row (AF4: to four rows).
 //  * Reduction: each lane has one value per (input row, chunk row of its
 //    group); a transposing butterfly adds them across the warp, and the WG
 //    warps of the group add their partial sums in warp order through shared
@@ -654,15 +659,15 @@ __device__ __forceinline__ void xreg_body(const Params& p, const CUtensorMap* mq
                 prefill::tma_load_2d(smem_addr(dst + p.sb_off), mm, (ch.row0 & 63) * 4,
                                      (ch.row0 >> 6) * (p.units >> 1), bar);
             } else {
-            const uint32_t qb = (uint32_t)(ch.n * p.row_bytes);
-            const uint32_t sbb = kAffine ? (uint32_t)(ch.n * p.G * 4) : 0u;
-            mbar_arrive_expect_tx(bar, qb + 2u * sbb);
-            bulk_g2s(smem_addr(dst), p.w[ch.wi] + (long long)ch.row0 * p.row_bytes, qb, bar, pol);
-            if (kAffine) {
-                const long long go = (long long)ch.row0 * p.G;
-                bulk_g2s(smem_addr(dst + p.sb_off), p.s + go, sbb, bar, pol);
-                bulk_g2s(smem_addr(dst + p.sb_off + p.RC * p.G * 4), p.b + go, sbb, bar, pol);
-            }
+                const uint32_t qb = (uint32_t)(ch.n * p.row_bytes);
+                const uint32_t sbb = kAffine ? (uint32_t)(ch.n * p.G * 4) : 0u;
+                mbar_arrive_expect_tx(bar, qb + 2u * sbb);
+                bulk_g2s(smem_addr(dst), p.w[ch.wi] + (long long)ch.row0 * p.row_bytes, qb, bar, pol);
+                if (kAffine) {
+                    const long long go = (long long)ch.row0 * p.G;
+                    bulk_g2s(smem_addr(dst + p.sb_off), p.s + go, sbb, bar, pol);
+                    bulk_g2s(smem_addr(dst + p.sb_off + p.RC * p.G * 4), p.b + go, sbb, bar, pol);
+                }
             }
             issued = i + 1;
             if (i == p.S - 1 || r == re) {
