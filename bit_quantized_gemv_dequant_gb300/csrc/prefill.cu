@@ -25,20 +25,26 @@
 //         makes the factored sum equal sum_k w * xh up to f32 rounding, so the
 //         error is at most 2^-11 * sum_k |w * x| plus f32 rounding.
 //   main: one CTA per (128 weight rows) x (128 activation rows) tile.
-//         warp 12      TMA producer: per 64-wide k chunk, the code tile
+//         warp 12      TMA producer: per 64-wide k sub-stage, the code tile
 //                      (128 rows, u8 or packed) and the xh tile (128 rows,
-//                      fp16, 128-byte swizzle) into a ring of stages.
+//                      fp16, 128-byte swizzle) into a ring of sub-stages;
+//                      two sub-stages (a 128-wide step) complete on one
+//                      barrier.
 //         warps 0-3    converters: codes -> fp16 (exact) in registers, stored
 //                      into tensor memory as the A operand (tcgen05.st); the
 //                      converted weights never pass through shared memory.
+//                      One A buffer (64 columns) per step, two buffers.
 //         warp 13      MMA issuer: kind::f16, M=128 (weight rows), N=128
-//                      (activation rows), K=16 per instruction, f32
-//                      accumulators P_g in tensor memory, three buffers.
+//                      (activation rows), K=16 per instruction, eight per
+//                      step, f32 accumulators P_g in tensor memory, three
+//                      buffers; it waits for the epilogue to release a P
+//                      buffer before a group starts in it.
 //         warps 4-11   epilogue: acc += s * P_g + b * X_g per group, in f32
 //                      registers (scales and biases read four groups
-//                      ahead); at the end y = acc * 2^-e_m. A converter fills
-//                      group i's A buffer only once the epilogue has released
-//                      P buffer i - 3: that cycle bounds the kernel.
+//                      ahead); at the end y = acc * 2^-e_m.
+//       Every barrier wait, fence and commit of the converters and the MMA
+//       thread is paid once per 128-wide step: measured, these hand-offs, not
+//       the copies or the arithmetic, bounded the kernel with 64-wide ones.
 // Every wait is bounded; a wait that runs out records an error bit and the
 // CTA winds down (drains its copies and MMAs, frees tensor memory) instead of
 // hanging.
@@ -50,11 +56,12 @@
 namespace qg {
 namespace prefill {
 
-constexpr int kStages = 8;
-constexpr int kABufs = 4;      // A operand buffers in tensor memory (32 columns each)
+constexpr int kStages = 8;     // 64-wide sub-stages in the shared-memory ring
+constexpr int kSteps = kStages / 2;  // 128-wide steps: two sub-stages per barrier
+constexpr int kABufs = 2;      // A operand buffers in tensor memory (64 columns each)
 constexpr int kPBufs = 3;      // P_g accumulators in tensor memory
 constexpr int kPCols = kTileT; // columns per P buffer
-constexpr int kACol0 = kPBufs * kPCols;  // A buffers follow: 384 + 4 * 32 = 512 columns
+constexpr int kACol0 = kPBufs * kPCols;  // A buffers follow: 384 + 2 * 64 = 512 columns
 constexpr int kXSlots = 32;    // ring of per-group activation sums in shared memory
 constexpr int kXSlotBytes = kTileT * 4;
 constexpr int kEpiWarps = 8;  // epilogue warps 4 .. 4 + kEpiWarps - 1
@@ -71,7 +78,7 @@ struct Params {
     const float* inv;      // [Mp] 2^-e_m
     int M, N, K, G, Mp;
     int gs;                // group size
-    int spgs;              // 64-wide stages per group when gs >= 64 (else 1)
+    int spgs;              // 128-wide steps per group when gs >= 128 (else 1)
     unsigned* err;
 };
 
@@ -245,8 +252,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(
 }
 
 // ------------------------------------------------------------- main kernel
-// GK: MMA k-steps (16 wide) per group when a group fits in one stage
-// (gs = 16 -> 1, gs = 32 -> 2), or 4 when a group spans whole stages (gs >= 64).
+// GK: MMA k-steps (16 wide) per group when a group fits in one 128-wide step
+// (gs = 16, 32, 64 -> 1, 2, 4), or 8 when a group spans whole steps (gs >= 128).
 template <bool PACKED, int GK>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_x,
@@ -277,11 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * kTileT;
     const int n0 = blockIdx.y * kTileN;
-    const int nstages = (p.K + kChunk - 1) / kChunk;
+    const int nsub = (p.K + kChunk - 1) / kChunk;            // 64-wide sub-stages
+    const int nsteps = (nsub + 1) / 2;                         // 128-wide steps
     const int nks = p.K >> 4;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kSteps; ++i) {
             mbar_init(full(i), 1);
             mbar_init(empty(i), 1);
         }
@@ -319,19 +327,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&map_x);
             int issued = 0, xissued = 0;
             bool dead = false;
-            for (int i = 0; i < nstages && !dead; ++i) {
-                const int st = i % kStages;
-                if (i >= kStages && !mbar_wait(empty(st), ((i / kStages) & 1) ^ 1)) {
+            for (int i = 0; i < nsteps && !dead; ++i) {
+                const int t = i % kSteps;
+                if (i >= kSteps && !mbar_wait(empty(t), ((i / kSteps) & 1) ^ 1)) {
                     report_error(p.err, DEVERR_TC_WAIT);
                     break;
                 }
-                const uint32_t sb = base + st * Gm::kStageBytes;
-                mbar_arrive_expect_tx(full(st), Gm::kStageBytes);
-                tma_load_2d(sb, &map_x, i * kChunk, m0, full(st));
-                tma_load_2d(sb + kXhBytes, &map_q, i * Gm::kCodeRowBytes, n0, full(st));
+                // Step i: sub-stages 2i and 2i + 1 (the last step of a K
+                // that is an odd number of 64s has one) in ring regions 2t, 2t + 1.
+                const int ns = min(2, nsub - 2 * i);
+                mbar_arrive_expect_tx(full(t), (uint32_t)(ns * Gm::kStageBytes));
+                for (int sub = 0; sub < ns; ++sub) {
+                    const uint32_t sb = base + (2 * t + sub) * Gm::kStageBytes;
+                    tma_load_2d(sb, &map_x, (2 * i + sub) * kChunk, m0, full(t));
+                    tma_load_2d(sb + kXhBytes, &map_q, (2 * i + sub) * Gm::kCodeRowBytes, n0,
+                                full(t));
+                }
                 issued = i + 1;
-                // Activation sums of the groups that start inside this chunk.
-                const int ke = min(p.K, (i + 1) * kChunk);
+                // Activation sums of the groups that start inside this step.
+                const int ke = min(p.K, (i + 1) * 2 * kChunk);
                 for (int j = xissued; j * p.gs < ke; ++j) {
                     const int sl = j % kXSlots;
                     if (j >= kXSlots && !mbar_wait(x_empty(sl), ((j / kXSlots) & 1) ^ 1)) {
@@ -346,8 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Copies must land before the CTA can exit, whatever happened above.
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                if (!mbar_wait(full(i % kStages), (i / kStages) & 1))
+            for (int i = max(0, issued - kSteps); i < issued; ++i)
+                if (!mbar_wait(full(i % kSteps), (i / kSteps) & 1))
                     report_error(p.err, DEVERR_WAIT_DRAIN);
             for (int j = max(0, xissued - kXSlots); j < xissued; ++j)
                 if (!mbar_wait(x_full(j % kXSlots), (j / kXSlots) & 1))
@@ -359,27 +373,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // counters, k-steps unrolled): every instruction between two MMAs
         // of the single issuing thread delays the tensor pipe.
         if (lane == 0) {
-            int st = 0, ab = 0, pb = 0, gst = 0, groups = 0;
+            int t = 0, ab = 0, pb = 0, gst = 0, groups = 0;
             uint32_t aph = 0, pph = 0;
             bool dead = false;
-            for (int i = 0; i < nstages && !dead; ++i) {
-                const int nk = min(4, nks - 4 * i);
-                // a_full implies the stage's copies landed (the converters waited for
-                // them) and, for groups of 64 or more, that the P buffers the stage
-                // starts are free (the converters waited for those too): one barrier
-                // poll per stage, since each poll stalls the issuing thread.
+            for (int i = 0; i < nsteps && !dead; ++i) {
+                const int nk = min(8, nks - 8 * i);
+                // a_full implies the step's copies landed (the converters
+                // waited for them): one barrier poll per 128-wide step.
                 if (!mbar_wait(a_full(ab), aph)) {
                     report_error(p.err, DEVERR_TC_WAIT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sb = base + st * Gm::kStageBytes;
-                const uint32_t aa = tmem + kACol0 + ab * 32;
+                const uint32_t sb0 = base + (2 * t) * Gm::kStageBytes;
+                const uint32_t aa = tmem + kACol0 + ab * 64;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    if (GK < 4 && kk >= nk) break;
-                    const bool gstart = (GK == 4) ? (kk == 0 && gst == 0) : (kk % GK == 0);
-                    if (GK < 4 && gstart && groups >= kPBufs) {
+                for (int kk = 0; kk < 8; ++kk) {
+                    if (kk >= nk) break;
+                    const bool gstart = (GK == 8) ? (kk == 0 && gst == 0) : (kk % GK == 0);
+                    // A group's P buffer must have been drained by the epilogue.
+                    if (gstart && groups >= kPBufs) {
                         if (!mbar_wait(p_empty(pb), pph ^ 1)) {
                             report_error(p.err, DEVERR_TC_WAIT);
                             dead = true;
@@ -387,21 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                     }
-                    tc_mma_ts(tmem + pb * kPCols, aa + kk * 8, sw128_desc(sb + kk * 32), kIdesc,
+                    tc_mma_ts(tmem + pb * kPCols, aa + kk * 8,
+                              sw128_desc(sb0 + (kk >> 2) * Gm::kStageBytes + (kk & 3) * 32), kIdesc,
                               gstart ? 0u : 1u);
                     const bool gend =
-                        (GK == 4) ? (kk == 3 && gst == p.spgs - 1) : (kk % GK == GK - 1);
+                        (GK == 8) ? (kk == 7 && gst == p.spgs - 1) : (kk % GK == GK - 1);
                     if (gend) {
                         tc_commit(p_full(pb));
                         ++groups;
                         if (++pb == kPBufs) { pb = 0; pph ^= 1; }
                     }
                 }
-                tc_commit(empty(st));
+                tc_commit(empty(t));
                 tc_commit(a_empty(ab));
-                if (++st == kStages) st = 0;
+                if (++t == kSteps) t = 0;
                 if (++ab == kABufs) { ab = 0; aph ^= 1; }
-                if (GK == 4 && ++gst == p.spgs) gst = 0;
+                if (GK == 8 && ++gst == p.spgs) gst = 0;
             }
             tc_commit(done_bar);
             if (!mbar_wait(done_bar, 0)) report_error(p.err, DEVERR_WAIT_DRAIN);
@@ -410,66 +424,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- converters
         const int row = threadIdx.x;  // 0..127: lane 32*warp + lane of tensor memory
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        int st = 0, ab = 0, gst = 0, groups = 0, pb = 0;
-        uint32_t fph = 0, aph = 0, pph = 0;
-        for (int i = 0; i < nstages; ++i) {
-            if (!warp_wait(full(st), fph) || (i >= kABufs && !warp_wait(a_empty(ab), aph ^ 1))) {
+        int t = 0, ab = 0;
+        uint32_t fph = 0, aph = 0;
+        for (int i = 0; i < nsteps; ++i) {
+            if (!warp_wait(full(t), fph) || (i >= kABufs && !warp_wait(a_empty(ab), aph ^ 1))) {
                 if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
                 break;
             }
             tc_fence_after();
-            const uint8_t* cb = smem + st * Gm::kStageBytes + kXhBytes;
-            const uint32_t acol = tmem + lane_base + kACol0 + ab * 32;
+            const int ns = min(2, nsub - 2 * i);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t h[16];
-                if (!PACKED) {
-                    // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+            for (int sub = 0; sub < 2; ++sub) {
+                if (sub >= ns) break;
+                const uint8_t* cb = smem + (2 * t + sub) * Gm::kStageBytes + kXhBytes;
+                const uint32_t acol = tmem + lane_base + kACol0 + ab * 64 + sub * 32;
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * hf + cc;
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t h[16];
+                    if (!PACKED) {
+                        // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = 2 * hf + cc;
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                cb + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                            codes4_to_h2(v.x, h[8 * cc + 0], h[8 * cc + 1]);
+                            codes4_to_h2(v.y, h[8 * cc + 2], h[8 * cc + 3]);
+                            codes4_to_h2(v.z, h[8 * cc + 4], h[8 * cc + 5]);
+                            codes4_to_h2(v.w, h[8 * cc + 6], h[8 * cc + 7]);
+                        }
+                    } else {
+                        // 32-byte swizzle: chunk c of row r sits at chunk c ^ ((r >> 2) & 1).
                         const uint4 v = *reinterpret_cast<const uint4*>(
-                            cb + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
-                        codes4_to_h2(v.x, h[8 * cc + 0], h[8 * cc + 1]);
-                        codes4_to_h2(v.y, h[8 * cc + 2], h[8 * cc + 3]);
-                        codes4_to_h2(v.z, h[8 * cc + 4], h[8 * cc + 5]);
-                        codes4_to_h2(v.w, h[8 * cc + 6], h[8 * cc + 7]);
-                    }
-                } else {
-                    // 32-byte swizzle: chunk c of row r sits at chunk c ^ ((r >> 2) & 1).
-                    const uint4 v = *reinterpret_cast<const uint4*>(
-                        cb + row * 32 + ((hf ^ ((row >> 2) & 1)) << 4));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                            cb + row * 32 + ((hf ^ ((row >> 2) & 1)) << 4));
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // low nibble of each byte = even k, high nibble = odd k
-                        const uint32_t lo = w4[e] & 0x0F0F0F0Fu;
-                        const uint32_t hi = (w4[e] >> 4) & 0x0F0F0F0Fu;
-                        codes4_to_h2(__byte_perm(lo, hi, 0x5140u), h[4 * e + 0], h[4 * e + 1]);
-                        codes4_to_h2(__byte_perm(lo, hi, 0x7362u), h[4 * e + 2], h[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e) {
+                            // low nibble of each byte = even k, high nibble = odd k
+                            const uint32_t lo = w4[e] & 0x0F0F0F0Fu;
+                            const uint32_t hi = (w4[e] >> 4) & 0x0F0F0F0Fu;
+                            codes4_to_h2(__byte_perm(lo, hi, 0x5140u), h[4 * e + 0], h[4 * e + 1]);
+                            codes4_to_h2(__byte_perm(lo, hi, 0x7362u), h[4 * e + 2], h[4 * e + 3]);
+                        }
                     }
+                    tmem_st16(acol + hf * 16, h);
                 }
-                tmem_st16(acol + hf * 16, h);
             }
             tmem_st_wait();
-            if (GK == 4 && gst == 0) {
-                // This stage starts a group: its P buffer must be drained first.
-                if (groups >= kPBufs && !warp_wait(p_empty(pb), pph ^ 1)) {
-                    if (lane == 0) report_error(p.err, DEVERR_TC_WAIT);
-                    break;
-                }
-                ++groups;
-                if (++pb == kPBufs) { pb = 0; pph ^= 1; }
-            }
             // One arrival per warp: the barrier sees 4 arrivals instead of 128
             // serialised ones. The warp's tensor-memory stores are ordered
             // before it by the fence and the warp barrier.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full(ab));
-            if (++st == kStages) { st = 0; fph ^= 1; }
+            if (++t == kSteps) { t = 0; fph ^= 1; }
             if (++ab == kABufs) { ab = 0; aph ^= 1; }
-            if (GK == 4 && ++gst == p.spgs) gst = 0;
         }
     } else if (warp < 4 + kEpiWarps) {
         // ------------------------------------------------------------ epilogue
@@ -764,7 +773,7 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
     kp.G = L.G;
     kp.Mp = L.Mp;
     kp.gs = a.gs;
-    kp.spgs = a.gs >= kChunk ? a.gs / kChunk : 1;
+    kp.spgs = a.gs >= 2 * kChunk ? a.gs / (2 * kChunk) : 1;  // steps per group (gs >= 128)
     kp.err = dc.err;
     if (a.gs == 16)
         return packed ? launch_main<true, 1>(dc, mq, mx, kp, grid, s)
@@ -772,8 +781,11 @@ int prefill_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_byte
     if (a.gs == 32)
         return packed ? launch_main<true, 2>(dc, mq, mx, kp, grid, s)
                       : launch_main<false, 2>(dc, mq, mx, kp, grid, s);
-    return packed ? launch_main<true, 4>(dc, mq, mx, kp, grid, s)
-                  : launch_main<false, 4>(dc, mq, mx, kp, grid, s);
+    if (a.gs == 64)
+        return packed ? launch_main<true, 4>(dc, mq, mx, kp, grid, s)
+                      : launch_main<false, 4>(dc, mq, mx, kp, grid, s);
+    return packed ? launch_main<true, 8>(dc, mq, mx, kp, grid, s)
+                  : launch_main<false, 8>(dc, mq, mx, kp, grid, s);
 }
 
 }  // namespace qg
