@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import math
 import os
@@ -435,13 +436,18 @@ def e2e_dual(steps: int, warmup: int, M: int = 1, N: int = 4096, K: int = 4096):
     memory) and returns once the outputs hold the result. Also reported: the
     same call on pageable buffers (one cudaMemcpyAsync per buffer through
     device staging), and the device-resident call followed by a stream
-    synchronize (the launch and the host round trip alone)."""
+    synchronize (the launch and the host round trip alone). Steps rotate
+    over the same weight sets as the headline (more than 4x the L2), so
+    every step streams its weights from HBM."""
     import torch
     import bit_quantized_gemv_dequant_gb300 as qg
     from bit_quantized_gemv_dequant_gb300 import synth
     dev = torch.device("cuda", torch.cuda.current_device())
     c = synth.q4_0_case(1, N, K, M, dual=True)
-    wa, wb = torch.from_numpy(c["w"]).to(dev), torch.from_numpy(c["w_b"]).to(dev)
+    et = 2 * N * q4_0_row_bytes(K) + 4 * M * K + 2 * 4 * M * N
+    ns = n_sets(et)
+    wa = replicate(torch.from_numpy(c["w"]).to(dev), ns)
+    wb = replicate(torch.from_numpy(c["w_b"]).to(dev), ns)
     x_pin = torch.from_numpy(c["x"]).pin_memory()
     y_pin = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _ in range(2)]
     x_page = torch.from_numpy(c["x"]).clone()
@@ -453,21 +459,26 @@ def e2e_dual(steps: int, warmup: int, M: int = 1, N: int = 4096, K: int = 4096):
     h = stream.cuda_stream
     need = qg.workspace_size(qg.QG_OP_DUAL_Q4_0_HOST, M, N, K)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-    pa, pb, pws = wa.data_ptr(), wb.data_ptr(), ws.data_ptr()
+    pws = ws.data_ptr()
+    wp = [(wa[i].data_ptr(), wb[i].data_ptr()) for i in range(ns)]
 
     def host_call(x, ya, yb):
-        args = (pa, pb, x.data_ptr(), ya.data_ptr(), yb.data_ptr(), M, N, K, pws, need, h)
+        args = [(pa, pb, x.data_ptr(), ya.data_ptr(), yb.data_ptr(), M, N, K, pws, need, h)
+                for pa, pb in wp]
+        it = itertools.count()
 
         def step():
-            rc = L.qgemv_dual_q4_0_host(*args)
+            rc = L.qgemv_dual_q4_0_host(*args[next(it) % ns])
             if rc:
                 raise RuntimeError(f"qgemv_dual_q4_0_host failed: {qg.status_string(rc)}")
         return step
 
-    dargs = (pa, pb, x_dev.data_ptr(), y_dev[0].data_ptr(), y_dev[1].data_ptr(), M, N, K, None, 0, h)
+    dargs = [(pa, pb, x_dev.data_ptr(), y_dev[0].data_ptr(), y_dev[1].data_ptr(), M, N, K, None,
+              0, h) for pa, pb in wp]
+    dit = itertools.count()
 
     def device_call():
-        rc = L.qgemv_dual_q4_0(*dargs)
+        rc = L.qgemv_dual_q4_0(*dargs[next(dit) % ns])
         if rc:
             raise RuntimeError(f"qgemv_dual_q4_0 failed: {qg.status_string(rc)}")
         stream.synchronize()
@@ -489,7 +500,6 @@ def e2e_dual(steps: int, warmup: int, M: int = 1, N: int = 4096, K: int = 4096):
         for got in (y_pin[i], y_page[i]):
             if not np.array_equal(got.numpy().view(np.uint32), ref):
                 raise RuntimeError("e2e: host-buffer result differs from the device call")
-    et = 2 * N * q4_0_row_bytes(K) + 4 * M * K + 2 * 4 * M * N
     us = out["pinned"]
     return {"value": et / (us * 1e3), "unit": "GB/s", "us_per_step": us, "steps": steps,
             "h2d_bytes_per_step": 4 * M * K, "d2h_bytes_per_step": 2 * 4 * M * N,
@@ -498,6 +508,7 @@ def e2e_dual(steps: int, warmup: int, M: int = 1, N: int = 4096, K: int = 4096):
                 "same call, pageable buffers (cudaMemcpyAsync through device staging)":
                     out["pageable"],
                 "device-resident call + stream synchronize (no host data)": out["device"]},
+            "weight_sets": ns,
             "how": "one qgemv_dual_q4_0_host call per step through ctypes: a fetch kernel "
                    "copies x from page-locked host memory into the workspace, the GEMV follows "
                    "as its programmatic dependent and stores y_a and y_b into page-locked host "
