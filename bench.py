@@ -796,7 +796,7 @@ def main():
                             "peak_source": f"{n_sm} SMs x 128 f32 FMA/clk x 2 x max SM clock"}})
     out["m8"] = m8
 
-    out["e2e"] = e2e_dual(min(2000, max(200, args.steps // 100)), 20)
+    out["e2e"] = e2e_dual(2000, 50)
 
     if not args.no_cpu:
         gbs1, rows1, calls1, dt1 = oracle_dual_sample(1, 4096, 4096, budget_s=6.0)
