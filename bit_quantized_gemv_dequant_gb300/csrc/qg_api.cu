@@ -572,7 +572,8 @@ int qg_set_option(int option, int64_t value) {
         case QG_OPT_XREG_WARPS:
             if (value != 0 && value != 4 && value != 8 && value != 16) return QG_ERR_INVALID_ARG;
             g_opt_xreg_warps.store(value, std::memory_order_relaxed);
-            return QG_OK;        case QG_OPT_XREG_CTAS:
+            return QG_OK;
+        case QG_OPT_XREG_CTAS:
             if (value < 1 || value > 4) return QG_ERR_INVALID_ARG;
             g_opt_xreg_ctas.store(value, std::memory_order_relaxed);
             return QG_OK;
