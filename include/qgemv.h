@@ -134,14 +134,18 @@ QG_API int qgemv_dual_q4_0(const void* w_a, const void* w_b, const float* x, flo
  * - Zero-copy: when x, y_a and y_b are page-locked host memory mapped for the
  *   device (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped),
  *   x is 16-byte aligned, and every slice of the call runs on the
- *   register-resident-x kernel (M <= 2 for this format), the kernel reads x
- *   and writes y_a, y_b in host memory directly (plain loads and stores over
- *   the host link); nothing else is enqueued and no workspace is used.
+ *   register-resident-x kernel (M <= 2 for this format), a small kernel
+ *   copies x from host memory into the workspace and the GEMV, launched as
+ *   its programmatic dependent, reads x there and writes y_a and y_b straight
+ *   into host memory (plain stores over the host link). No copy-engine
+ *   transfer is enqueued.
  * - Otherwise (pageable buffers, other M): x is copied into the workspace,
  *   the call runs there and y_a, y_b are copied back, each with one
- *   cudaMemcpyAsync on `stream`. workspace: device memory of at least
+ *   cudaMemcpyAsync on `stream`.
+ * - workspace: device memory of at least
  *   qg_workspace_size(QG_OP_DUAL_Q4_0_HOST, M, N, K, 0, 0) bytes, 16-byte
- *   aligned; QG_ERR_WORKSPACE (nothing enqueued) when it is smaller.
+ *   aligned, on both routes (the staging of x, y_a and y_b sits at its end);
+ *   QG_ERR_WORKSPACE (nothing enqueued) when it is smaller.
  * - Host buffers must not overlap one another. Errors as for
  *   qgemv_dual_q4_0; a failed copy or synchronization returns QG_ERR_CUDA. */
 QG_API int qgemv_dual_q4_0_host(const void* w_a, const void* w_b, const float* x, float* y_a,
