@@ -33,7 +33,7 @@ std::atomic<long long> g_opt_prefill_fold{0};
 std::atomic<long long> g_opt_xreg{1};
 std::atomic<long long> g_opt_xreg_ahead{0};
 std::atomic<long long> g_opt_xreg_warps{0};
-std::atomic<long long> g_opt_xreg_ctas{1};
+std::atomic<long long> g_opt_xreg_ctas{0};
 
 int init_ctx(int dev) {
     DevCtx& c = g_ctx[dev];
@@ -574,7 +574,7 @@ int qg_set_option(int option, int64_t value) {
             g_opt_xreg_warps.store(value, std::memory_order_relaxed);
             return QG_OK;
         case QG_OPT_XREG_CTAS:
-            if (value < 1 || value > 4) return QG_ERR_INVALID_ARG;
+            if (value < 0 || value > 4) return QG_ERR_INVALID_ARG;
             g_opt_xreg_ctas.store(value, std::memory_order_relaxed);
             return QG_OK;
         default: return QG_ERR_INVALID_ARG;

@@ -335,14 +335,16 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * of weights the register-resident-x kernel keeps in flight at most (tuning).
  *
  * QG_OPT_XREG_WARPS (default 0 = automatic; or 4, 8, 16) and
- * QG_OPT_XREG_CTAS (default 1; 1..4): consumer warps per CTA and CTAs per SM
- * per call of the register-resident-x kernel (tuning; results are bitwise
- * the same). A count that does not suit the shape (the warps of one row
- * group must divide it; sixteen warps take one x row) falls back to
- * automatic. With four consumer warps (rows of at most 4096 weights of K),
- * four CTAs share an SM; automatic picks them when QG_OPT_PDL is 2, eight
- * warps otherwise and for the host-buffer call (a lone call, which also
- * takes all of the SM's shared memory). */
+ * QG_OPT_XREG_CTAS (default 0 = automatic; or 1..4): consumer warps per CTA
+ * and CTAs per SM per call of the register-resident-x kernel (tuning;
+ * results are bitwise the same). A count that does not suit the shape (the
+ * warps of one row group must divide it; sixteen warps take one x row) falls
+ * back to automatic. With four consumer warps (rows of at most 4096 weights
+ * of K), four CTAs share an SM; automatic picks them when QG_OPT_PDL is 2,
+ * eight warps otherwise and for the host-buffer call (a lone call, which
+ * also takes all of the SM's shared memory). Automatic CTAs: one per two
+ * SMs per call when QG_OPT_PDL is 2 (the calls' CTAs overlap), one per SM
+ * otherwise. */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
        QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6, QG_OPT_STAGED_WARPS = 7,
        QG_OPT_PREFILL_FOLD = 8, QG_OPT_XREG = 9, QG_OPT_XREG_AHEAD = 10,

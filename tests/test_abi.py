@@ -111,7 +111,7 @@ def test_launch_options_round_trip_and_validation(lib):
              9: ([0, 1], [2, -1]),            # QG_OPT_XREG
              10: ([0, 1, 16], [17, -1]),      # QG_OPT_XREG_AHEAD
              11: ([4, 8, 16, 0], [2, 12, -1]),  # QG_OPT_XREG_WARPS
-             12: ([2, 4, 1], [0, 5])}         # QG_OPT_XREG_CTAS
+             12: ([2, 4, 1, 0], [-1, 5])}     # QG_OPT_XREG_CTAS
     for opt, (good, bad) in cases.items():
         rc, old = get(opt)
         assert rc == 0

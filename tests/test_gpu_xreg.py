@@ -276,14 +276,14 @@ def test_xreg_cta_shape_does_not_change_results():
     try:
         for warps in (4, 8, 16):
             qg.set_option(qg.QG_OPT_XREG_WARPS, warps)
-            for ctas in (1, 2, 4):
+            for ctas in (0, 1, 2, 4):
                 qg.set_option(qg.QG_OPT_XREG_CTAS, ctas)
                 ya, yb = qg.qgemv_dual_q4_0(wa, wb, x, N=N)
                 assert_bitwise(ya, base[0], f"{warps} warps, {ctas} CTAs per SM, y_a")
                 assert_bitwise(yb, base[1], f"{warps} warps, {ctas} CTAs per SM, y_b")
     finally:
         qg.set_option(qg.QG_OPT_XREG_WARPS, 0)
-        qg.set_option(qg.QG_OPT_XREG_CTAS, 1)
+        qg.set_option(qg.QG_OPT_XREG_CTAS, 0)
 
 
 @pytest.mark.parametrize("M", [3, 4, 5, 7, 8, 11])
