@@ -451,21 +451,24 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // (their results are bitwise equal only then): whether the plan fits is
     // decided on the larger, one-code-per-byte slot for both.
     const long long slot_fit = affine ? ((RC * a.K + 2ll * RC * G * 4) + 127) & ~127ll : slot;
-    // Rows of per-warp partial sums buffered before a flush: the CTA's whole
-    // share when it fits in 16 KB, and never fewer than one chunk.
     // CTAs per call: one per two SMs for calls declared independent
-    // (QG_OPT_PDL = 2), whose CTAs overlap those of the calls around them:
-    // fewer, longer CTAs spend less per call on start-up and x staging
-    // (measured: the dual N = K = 4096 call 3.55 against 3.83 us, Q4_K
-    // N = 4096 2.32 against 2.51, M = 2 K+V 1.75 against 2.37, over runs of
-    // hundreds of calls). One per SM for a call that waits for its
-    // predecessor or runs alone, which has the GPU to itself.
+    // (QG_OPT_PDL = 2) whose CTAs share SMs with those of the calls around
+    // them (the shapes that fit two or more CTAs on an SM): fewer, longer
+    // CTAs spend less per call on start-up and x staging (measured: the dual
+    // N = K = 4096 call 3.55 against 3.83 us, Q4_K N = 4096 2.32 against
+    // 2.51, M = 2 K+V 1.75 against 2.37, over runs of hundreds of calls).
+    // One per SM for a call that waits for its predecessor or runs alone,
+    // and for the one-CTA-per-SM shapes (four rows of x).
+    const bool shares_sm = ((NWC == 8 || NWC == 12) && MT == 1) || (NWC == 4 && MT <= 2);
     const long long ctas_opt = launch_option(QG_OPT_XREG_CTAS);
-    const bool overlapped = !a.isolated && !a.x_from_prev && launch_option(QG_OPT_PDL) == 2;
+    const bool overlapped =
+        shares_sm && !a.isolated && !a.x_from_prev && launch_option(QG_OPT_PDL) == 2;
     const long long grid_max = ctas_opt > 0 ? (long long)dc.num_sms * ctas_opt
                                : overlapped ? std::max<long long>(1, dc.num_sms / 2)
                                             : (long long)dc.num_sms;
     const long long rows_cta = ((long long)a.nw * a.N + grid_max - 1) / grid_max;
+    // Rows of per-warp partial sums buffered before a flush: the CTA's whole
+    // share when it fits in 16 KB, and never fewer than one chunk.
     const long long rbuf = std::max<long long>(RC, std::min<long long>(rows_cta, 4096 / (MT * WG)));
     const long long per_slot = slot + 16;
     // Partial sums, then the staging area of x (MT * K floats).
@@ -474,8 +477,7 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // Eight or twelve consumer warps with one input row fit twice on an SM
     // (this call's CTA and the next one's), four consumer warps four times
     // (three times with two input rows); otherwise one CTA per SM.
-    const bool co = !a.isolated &&
-                    (((NWC == 8 || NWC == 12) && MT == 1) || (NWC == 4 && MT <= 2));
+    const bool co = !a.isolated && shares_sm;
     const int per_sm = NWC == 4 ? (MT == 1 ? 4 : 3) : 2;
     long long budget = co ? (long long)dc.smem_per_sm / per_sm - dc.reserved_smem : dc.max_smem_optin;
     long long S = std::min<long long>(16, (budget - fixed) / per_slot);
