@@ -98,16 +98,16 @@ int af4_xreg_launch(const DevCtx& dc, const float* x, const uint32_t* plane,
 
     const long long pdl_mode = launch_option(QG_OPT_PDL);
     const long long want_w = launch_option(QG_OPT_XREG_WARPS);
-    // CTAs per call as in make_xreg_plan: for independent calls
-    // (QG_OPT_PDL = 2) on the automatic four-warp shape, whose CTAs share
-    // SMs with the neighbouring calls', three per four SMs for one row of x
-    // and one per two SMs for two; else one per SM, unless QG_OPT_XREG_CTAS
-    // sets it.
+    // CTAs per call: for independent calls (QG_OPT_PDL = 2) on the automatic
+    // four-warp shape, whose CTAs share SMs with the neighbouring calls', one
+    // per two SMs (M = 1, N = K = 4096, long runs: 2.00 us against 2.02 with
+    // three per four and 2.06 with one per SM); else one per SM, unless
+    // QG_OPT_XREG_CTAS sets it.
     const long long ctas_opt = launch_option(QG_OPT_XREG_CTAS);
     const long long quads = N / 4;
     const long long grid_max = ctas_opt > 0 ? (long long)dc.num_sms * ctas_opt
                                : (pdl_mode == 2 && want_w == 0)
-                                   ? std::max<long long>(1, dc.num_sms * (M == 1 ? 3 : 2) / 4)
+                                   ? std::max<long long>(1, dc.num_sms / 2)
                                    : (long long)dc.num_sms;
     const long long grid = std::min<long long>(quads, grid_max);
     const long long rows_cta = 4 * ((quads + grid - 1) / grid);
