@@ -451,22 +451,24 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // (their results are bitwise equal only then): whether the plan fits is
     // decided on the larger, one-code-per-byte slot for both.
     const long long slot_fit = affine ? ((RC * a.K + 2ll * RC * G * 4) + 127) & ~127ll : slot;
-    // CTAs per call. For calls declared independent (QG_OPT_PDL = 2) whose
-    // CTAs share SMs with those of the calls around them (the shapes that fit
-    // two or more CTAs on an SM), fewer, longer CTAs spend less per call on
-    // start-up and x staging: three per four SMs for one row of x on four
-    // warps, one per two SMs otherwise. Measured over runs of hundreds of
-    // calls (us per call, one per SM / three per four / one per two): dual
-    // N = K = 4096 3.83 / 3.61 / 3.55, Q4_K N = 12288 6.63 / 6.42 / 6.48,
-    // decode layer 22.2 / 21.0 / 21.5, M = 2 K+V 2.37 / 2.07 / 1.76; over
-    // 20 calls, where the longer CTAs' fill and drain count, the dual call
-    // 4.36-4.46 / 4.36 / 4.46. One per SM for a call that waits for its
-    // predecessor or runs alone, and for the one-CTA-per-SM shapes (four rows
-    // of x).
+    // CTAs per call. For calls with one or two rows of x declared
+    // independent (QG_OPT_PDL = 2), whose CTAs run beside those of the calls
+    // around them, fewer, longer CTAs spend less per call on start-up and x
+    // staging: three per four SMs for one row of x on four warps, one per two
+    // SMs otherwise. Measured over runs of hundreds of calls (us per call, one
+    // per SM / three per four / one per two): dual N = K = 4096 3.83 / 3.61 /
+    // 3.55, Q4_K N = 12288 6.63 / 6.42 / 6.48, decode layer 22.2 / 21.0 /
+    // 21.5, M = 2 K+V 2.37 / 2.07 / 1.76, M = 2 Q4_K K = 12288 14.9 / - /
+    // 12.1; over 20 calls, where the longer CTAs' fill and drain count, the
+    // dual call 4.36-4.46 / 4.36 / 4.46. One per SM for a call that waits for
+    // its predecessor or runs alone, and for four rows of x, whose calls run
+    // beside the staged kernel's single wave of CTAs (halving them made the
+    // M = 4 decode layer 93 us against 74: the staged CTAs waited for the
+    // longer ones to leave their SMs).
     const bool shares_sm = ((NWC == 8 || NWC == 12) && MT == 1) || (NWC == 4 && MT <= 2);
     const long long ctas_opt = launch_option(QG_OPT_XREG_CTAS);
     const bool overlapped =
-        shares_sm && !a.isolated && !a.x_from_prev && launch_option(QG_OPT_PDL) == 2;
+        MT <= 2 && !a.isolated && !a.x_from_prev && launch_option(QG_OPT_PDL) == 2;
     const long long quarters = (NWC == 4 && MT == 1) ? 3 : 2;  // SMs per call, in quarters
     const long long grid_max = ctas_opt > 0 ? (long long)dc.num_sms * ctas_opt
                                : overlapped ? std::max<long long>(1, dc.num_sms * quarters / 4)
