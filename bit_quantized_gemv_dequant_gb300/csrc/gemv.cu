@@ -740,6 +740,10 @@ int gemv_launch(const DevCtx& dc, const GemvArgs& a, void* ws, size_t ws_bytes, 
         kp.xsum_bytes = pl.xsum_bytes;
         kp.magic = 0x4B000000u;
         kp.err = dc.err;
+        // Independent calls (QG_OPT_PDL = 2) need not wait for their
+        // predecessor, except when split-K partials go to a workspace that
+        // consecutive calls may share.
+        kp.dep_wait = (launch_option(QG_OPT_PDL) == 2 && !a.x_from_prev && pl.KS == 1) ? 0 : 1;
         if (pl.KS > 1) {
             const size_t need = (size_t)pl.KS * a.nw * Mc * (size_t)a.N * sizeof(float);
             if (!ws || ws_bytes < need) return QG_ERR_WORKSPACE;

@@ -134,6 +134,7 @@ struct Params {
     int xs_bytes, xsum_bytes;
     uint32_t magic;            // 0x4B000000, passed in so it stays in a register
     unsigned* err;
+    int dep_wait;              // 1: wait for the preceding kernel before reading x / writing y
 };
 
 // 2^23 + bias * 2^s as the constant removed by the packed subtraction.
@@ -395,8 +396,10 @@ __global__ void __launch_bounds__((W + 1) * 32, (W == 8 && MT == 1) ? 2 : 1) gem
         return;
     }
 
-    // x and y may be produced / consumed by the preceding kernel.
-    pdl_wait();
+    // x and y may be produced / consumed by the preceding kernel (unless the
+    // caller declared the calls independent and no split-K workspace is in
+    // use).
+    if (p.dep_wait) pdl_wait();
 
     // ------------------------------------------------- stage x (consumers)
     // Shift-only index math: UE and PASS are powers of two. Every thread

@@ -278,10 +278,11 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * immediately preceding it on the stream writes, and writes nothing that
  * kernel reads or writes (independent projections, e.g. several projections
  * of one input, or calls on distinct buffers). The register-resident-x
- * kernel (QG_OPT_XREG) then does not wait for its predecessor at all, so
- * consecutive independent calls run concurrently, two CTAs per SM; the other
- * kernels behave as with 1. A kernel launched after such a call without
- * programmatic dependent launch still waits for it as usual. */
+ * kernel (QG_OPT_XREG) and the staged kernel (when the call needs no split-K
+ * workspace, which consecutive calls may share) then do not wait for their
+ * predecessor at all, so consecutive independent calls run concurrently; the
+ * other kernels behave as with 1. A kernel launched after such a call
+ * without programmatic dependent launch still waits for it as usual. */
 /*
  * QG_OPT_PREFILL_MIN_M (default 64, >= 1): smallest M for which qmm_affine
  * (and the Q4_0 / Q4_K calls) take the tensor-core prefill path when its
