@@ -455,12 +455,14 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     // independent (QG_OPT_PDL = 2), whose CTAs run beside those of the calls
     // around them, fewer, longer CTAs spend less per call on start-up and x
     // staging: three per four SMs for one row of x on four warps, one per two
-    // SMs otherwise. Measured over runs of hundreds of calls (us per call, one
-    // per SM / three per four / one per two): dual N = K = 4096 3.83 / 3.61 /
-    // 3.55, Q4_K N = 12288 6.63 / 6.42 / 6.48, decode layer 22.2 / 21.0 /
-    // 21.5, M = 2 K+V 2.37 / 2.07 / 1.76, M = 2 Q4_K K = 12288 14.9 / - /
-    // 12.1; over 20 calls, where the longer CTAs' fill and drain count, the
-    // dual call 4.36-4.46 / 4.36 / 4.46. One per SM for a call that waits for
+    // SMs for one row on more warps, one per four SMs for two rows. Measured
+    // over runs of hundreds of calls (us per call, one per SM / three per
+    // four / one per two / one per four): dual N = K = 4096 3.83 / 3.61 /
+    // 3.55 / 4.03, Q4_K N = 12288 6.63 / 6.42 / 6.48 / 7.54, decode layer
+    // 22.2 / 21.0 / 21.5 / 20.5; two rows: K+V 2.37 / 2.07 / 1.76 / 1.67, Q4_K
+    // K = 12288 14.9 / - / 12.1 / 9.8, decode layer 33.6 / - / 29.5 / 28.2;
+    // over 20 calls, where the longer CTAs' fill and drain count, the dual
+    // call 4.36-4.46 / 4.36 / 4.46 / 5.28. One per SM for a call that waits for
     // its predecessor or runs alone, and for four rows of x, whose calls run
     // beside the staged kernel's single wave of CTAs (halving them made the
     // M = 4 decode layer 93 us against 74: the staged CTAs waited for the
@@ -469,7 +471,7 @@ XPlan make_xreg_plan(const DevCtx& dc, const GemvArgs& a, int Mc, const float* x
     const long long ctas_opt = launch_option(QG_OPT_XREG_CTAS);
     const bool overlapped =
         MT <= 2 && !a.isolated && !a.x_from_prev && launch_option(QG_OPT_PDL) == 2;
-    const long long quarters = (NWC == 4 && MT == 1) ? 3 : 2;  // SMs per call, in quarters
+    const long long quarters = MT == 2 ? 1 : NWC == 4 ? 3 : 2;  // SMs per call, in quarters
     const long long grid_max = ctas_opt > 0 ? (long long)dc.num_sms * ctas_opt
                                : overlapped ? std::max<long long>(1, dc.num_sms * quarters / 4)
                                             : (long long)dc.num_sms;

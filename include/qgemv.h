@@ -346,7 +346,8 @@ QG_API int qg_workspace_size(int op, int64_t M, int64_t N, int64_t K, int group_
  * also takes all of the SM's shared memory). Automatic CTAs, when QG_OPT_PDL
  * is 2 and a slice has one or two rows of x (the calls' CTAs overlap): three
  * per four SMs per call for one row of x on four warps (one per two SMs for
- * qmm_af4_g64), one per two SMs otherwise; one per SM in every other case. */
+ * qmm_af4_g64), one per two SMs for one row on more warps, one per four SMs
+ * for two rows; one per SM in every other case. */
 enum { QG_OPT_PDL = 1, QG_OPT_PREFILL_MIN_M = 2, QG_OPT_STREAM = 3, QG_OPT_STREAM_WARPS = 4,
        QG_OPT_STREAM_SLOTS = 5, QG_OPT_STAGES_AHEAD = 6, QG_OPT_STAGED_WARPS = 7,
        QG_OPT_PREFILL_FOLD = 8, QG_OPT_XREG = 9, QG_OPT_XREG_AHEAD = 10,
